@@ -127,7 +127,8 @@ def e2m1_encode_scaled(x, scale) -> np.ndarray:
 
     ``scale`` is the decoded (already rounded) group scale and broadcasts
     against x. The nearest grid point g minimises |x| - g*scale| (exact in
-    float64: g*scale has at most 6 significant bits). A zero scale gives
+    float64: g*scale has at most 6 significant bits); |x| >= 6*scale gives
+    the largest magnitude. A zero scale gives
     magnitude code 0 for every value. The sign bit is copied from x."""
     x = np.asarray(x, dtype=np.float64)
     scale = np.broadcast_to(np.asarray(scale, dtype=np.float64), x.shape)
@@ -137,6 +138,10 @@ def e2m1_encode_scaled(x, scale) -> np.ndarray:
         a = np.abs(xc)
         dist = np.abs(a[:, None] - sc[:, None] * _E2M1_POS)
         mag = _nearest_even(dist).astype(np.uint8)
+        # saturation: at or beyond 6*S the largest magnitude is the answer
+        # (stated explicitly: far beyond 6*S the float64 distances to the
+        # grid points are all rounded to |x| and can no longer tell)
+        mag = np.where(a >= E2M1_MAX * sc, np.uint8(7), mag)
         mag = np.where(sc == 0.0, np.uint8(0), mag).astype(np.uint8)
         return mag | np.where(np.signbit(xc), np.uint8(8), np.uint8(0))
 

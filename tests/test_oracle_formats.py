@@ -111,12 +111,14 @@ def textbook_e2m1(y):
 
 def check_e2m1_encode_exhaustive():
     x = FINITE_BF16
-    x = x[np.abs(x) < 1e6]
     scales = formats.E4M3_TABLE[1:127]  # every non-zero finite scale
     rng = np.random.default_rng(0)
+    huge = x[np.abs(x) > 1e30]
     for S in scales:
-        # values in the range that matters for this scale, plus random others
-        xs = np.concatenate([x[(np.abs(x) <= 8 * S) & (np.abs(x) >= S / 8)], rng.choice(x, 256)])
+        # values in the range that matters for this scale, random others from
+        # the whole bf16 range, and the largest magnitudes (saturation)
+        xs = np.concatenate([x[(np.abs(x) <= 8 * S) & (np.abs(x) >= S / 8)], rng.choice(x, 256),
+                             rng.choice(huge, 64)])
         codes = formats.e2m1_encode_scaled(xs, S)
         ref = textbook_e2m1(xs / S)
         got = formats.E2M1_TABLE[codes & 7]

@@ -143,3 +143,18 @@ def test_transposed_page_offset(monkeypatch):
 
     monkeypatch.setattr(attention, "select_rows", mutated)
     assert fails(A.check_brute_force)
+
+
+def test_missing_saturation(monkeypatch):
+    """Nearest-grid search without the explicit saturation rule: float64
+    distances far beyond 6*S all round to |x| and the search picks code 0."""
+    def mutated(x, scale):
+        x = np.asarray(x, dtype=np.float64)
+        scale = np.broadcast_to(np.asarray(scale, dtype=np.float64), x.shape)
+        dist = np.abs(np.abs(x)[..., None] - scale[..., None] * formats.E2M1_TABLE[:8])
+        mag = formats._nearest_even(dist).astype(np.uint8)
+        mag = np.where(scale == 0, 0, mag).astype(np.uint8)
+        return (mag | np.where(np.signbit(x), 8, 0)).astype(np.uint8)
+
+    monkeypatch.setattr(formats, "e2m1_encode_scaled", mutated)
+    assert fails(F.check_e2m1_encode_exhaustive)
