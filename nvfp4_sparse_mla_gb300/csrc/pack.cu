@@ -1,0 +1,98 @@
+// nvfp4_mla_pack: quantise new tokens into 352-byte NVFP4 cache rows.
+//
+// "Prime Inference: Fast, Reliable Serving for Frontier Open Models",
+// section "Making room for low-latency decode": the 512-value latent is
+// stored as 4-bit values with one FP8 scale per 16 values, the 64-value RoPE
+// part stays FP8, 352 bytes per row.
+//
+// One warp per token. Lane l owns latent group l (16 values = 32 bytes of
+// bf16, read as two 16-byte loads, so a warp reads the token's 1 KiB latent
+// fully coalesced) and RoPE values 2l, 2l+1. The group's scale and codes are
+// computed in registers without any shuffle; the 352-byte row is assembled
+// in shared memory and written as 22 aligned 16-byte stores.
+//
+// Rounding, bit-exact with the definition:
+//  * scale = E4M3(amax / 6): fp32 division correctly rounded (__fdiv_rn), then
+//    the hardware's round-to-nearest-even saturating E4M3 conversion. amax is
+//    a bf16 value (8 significant bits); amax/6 is either exact or has an
+//    infinite binary expansion, so the fp32 rounding can never create or
+//    break an E4M3 tie: the two roundings equal one.
+//  * codes: |v| is compared with S times the E2M1 midpoints 0.25, 0.75, 1.25,
+//    1.75, 2.5, 3.5, 5 (products exact in fp32); at a midpoint the strict or
+//    non-strict comparison sends the value to the even code.
+#include "common.cuh"
+
+namespace nvmla {
+
+constexpr int kPackWarps = 8;
+
+__global__ void __launch_bounds__(kPackWarps * 32)
+nvfp4_pack_kernel(const __nv_bfloat16* __restrict__ latent, int64_t lat_stride,
+                  const __nv_bfloat16* __restrict__ rope, int64_t rope_stride,
+                  const int32_t* __restrict__ slot_mapping, int64_t n_tokens,
+                  uint8_t* __restrict__ cache, int64_t num_slots, int32_t* err_word) {
+  __shared__ __align__(16) uint8_t rowbuf[kPackWarps][kRowBytes];
+  const int lane = threadIdx.x & 31;
+  const int wib = threadIdx.x >> 5;
+  uint8_t* row = rowbuf[wib];
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kPackWarps;
+
+  for (int64_t n = static_cast<int64_t>(blockIdx.x) * kPackWarps + wib; n < n_tokens; n += nwarps) {
+    const int64_t slot = __ldg(slot_mapping + n);
+    if (slot < 0) continue;
+    if (slot >= num_slots) {
+      if (lane == 0) report_error(err_word, NVMLA_ERRW_PACK_SLOT, 1);
+      continue;
+    }
+    // ---- latent group `lane`
+    const uint4* src = reinterpret_cast<const uint4*>(latent + n * lat_stride + lane * 16);
+    const uint4 a = __ldg(src);
+    const uint4 b = __ldg(src + 1);
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w[i] & 0xffffu)));
+      amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w[i] >> 16)));
+    }
+    const float q = __fdiv_rn(amax, 6.0f);
+    const uint32_t sbyte = f32x2_to_e4m3x2(q, 0.f) & 0xffu;
+    const float S = __half2float(__ushort_as_half(static_cast<uint16_t>(e4m3x2_to_f16x2(static_cast<uint16_t>(sbyte)) & 0xffffu)));
+    const float t0 = 0.25f * S, t1 = 0.75f * S, t2 = 1.25f * S, t3 = 1.75f * S;
+    const float t4 = 2.5f * S, t5 = 3.5f * S, t6 = 5.0f * S;
+    uint32_t codes[2] = {0u, 0u};
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t bits = (i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xffffu);
+      const float x = fabsf(bf16_bits_to_f32(bits));
+      uint32_t m = (x > t0) + (x >= t1) + (x > t2) + (x >= t3) + (x > t4) + (x >= t5) + (x > t6);
+      m = (S == 0.f) ? 0u : m;
+      const uint32_t c = m | ((bits >> 12) & 8u);
+      codes[i >> 3] |= c << (4 * (i & 7));
+    }
+    *reinterpret_cast<uint2*>(row + 8 * lane) = make_uint2(codes[0], codes[1]);
+    row[kScaleOff + lane] = static_cast<uint8_t>(sbyte);
+    // ---- RoPE values 2*lane, 2*lane+1
+    const uint32_t rw = __ldg(reinterpret_cast<const uint32_t*>(rope + n * rope_stride) + lane);
+    const uint16_t r8 = f32x2_to_e4m3x2(bf16_bits_to_f32(rw & 0xffffu), bf16_bits_to_f32(rw >> 16));
+    *reinterpret_cast<uint16_t*>(row + kRopeOff + 2 * lane) = r8;
+    __syncwarp();
+    if (lane < kRowBytes / 16) {
+      reinterpret_cast<uint4*>(cache + slot * kRowBytes)[lane] = reinterpret_cast<const uint4*>(row)[lane];
+    }
+    __syncwarp();
+  }
+}
+
+cudaError_t launch_pack(const void* latent, int64_t lat_stride, const void* rope, int64_t rope_stride,
+                        const int32_t* slot_mapping, int64_t n_tokens, uint8_t* cache, int64_t num_pages,
+                        int32_t* err_word, cudaStream_t stream) {
+  const int64_t blocks_needed = (n_tokens + kPackWarps - 1) / kPackWarps;
+  const int blocks = static_cast<int>(blocks_needed < 152 * 16 ? blocks_needed : 152 * 16);
+  nvfp4_pack_kernel<<<blocks, kPackWarps * 32, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(latent), lat_stride, static_cast<const __nv_bfloat16*>(rope),
+      rope_stride, slot_mapping, n_tokens, cache, num_pages * kPage, err_word);
+  return cudaGetLastError();
+}
+
+}  // namespace nvmla

