@@ -1,0 +1,457 @@
+"""Benchmark of the NVFP4 sparse-MLA decode path on one GB300.
+
+Workload (default): the pages' decode point -- 15 query tokens of one
+sequence, 64 heads, 200K-token context in 64-token pages behind a shuffled
+block table, top-2048 distinct uniform positions per token, NVFP4 cache
+(352-byte rows). One step is one pass of the whole path: nvfp4_mla_pack of
+the step's 15 new tokens into fresh slots, then sparse_mla_decode of the 15
+query tokens. L2 (126 MB) is flushed before every step by writing a 256 MiB
+buffer. The metric is the decode call's device time (CUDA events on the
+launching stream), in microseconds per call.
+
+Printed: one JSON line (rank 0). `--impl reference` times the CPU oracle on
+the same workload instead (the reference arm of this build).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sparse-MLA NVFP4 decode µs/call & % roofline (15 q-tok × top-2048, 1 GB300)"
+UNIT = "us/call"
+FLUSH_BYTES = 256 << 20
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+WORKLOAD_DESC = ("decode_point: 15 query tokens (1 sequence) x top-2048 distinct uniform positions, 64 heads, "
+                 "200K-token context, 64-token pages, NVFP4 latent 512 + FP8 RoPE 64 (352 B/row)")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--kernel", default="auto", choices=["auto", "mma", "tcgen05"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-staged", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(PEAKS_FALLBACK), "fallback"
+
+
+def algorithmic(w):
+    """Algorithmic bytes and flops of one decode call: per valid slot one
+    352-byte row and 64 heads x (2*576 + 2*512) flops; plus the queries,
+    index lists, block table entries read, outputs and lse."""
+    valid = int((w.topk_idx >= 0).sum())
+    T, H, K = w.T, w.H, w.topk
+    rows = valid * 352
+    q = T * H * 576 * 2
+    idx = T * K * 4
+    bt = int(w.block_table.numel()) * 4
+    out = T * H * 512 * 2 + T * H * 4
+    flops = valid * H * (2 * 576 + 2 * 512)
+    return {"bytes": rows + q + idx + bt + out, "row_bytes": rows, "flops": flops, "valid_slots": valid}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def source_hash(names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "nvfp4_sparse_mla_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_record(kernel_files, launch_key):
+    """DRAM traffic per launch from a committed ncu summary, or None when the
+    kernel source changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    rec = d.get(launch_key)
+    if not rec or rec.get("source_hash") != source_hash(kernel_files):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def cpu_baseline(w, seconds: float):
+    """The oracle, as it stands, on the host cores: whole decode calls of the
+    same workload, repeated until `seconds` have elapsed (at least one)."""
+    import numpy as np
+    from oracle import attention as oatt
+    from oracle import pack as opack
+
+    lat, rope, slots = w.all_written()
+    cache = np.zeros((w.num_pages + 1, 64, 352), dtype=np.uint8)
+    opack.pack_into_cache(lat.double().numpy(), rope.double().numpy(), slots.numpy(), cache)
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oatt.sparse_mla_decode(w.q_latent, w.q_rope, cache, w.block_table, w.topk_idx, w.sm_scale,
+                               w.q_seq_idx, w.seq_lens)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    threads = blas_threads()
+    return {"value": el / n * 1e6, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{n} whole decode calls of the workload (15 tokens x 2048 slots each), "
+                      f"numpy float64 with a {threads}-thread BLAS on {os.cpu_count()} host cores"}
+
+
+def blas_threads():
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var):
+            try:
+                return int(os.environ[var])
+            except ValueError:
+                pass
+    try:
+        import threadpoolctl
+        info = threadpoolctl.threadpool_info()
+        if info:
+            return max(int(i.get("num_threads", 1)) for i in info)
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def run_reference(args, rank, world):
+    """Reference arm: the CPU oracle timed on this machine's host cores."""
+    if rank != 0:
+        return
+    from nvfp4_sparse_mla_gb300 import workloads
+    import numpy as np
+    from oracle import attention as oatt
+    from oracle import pack as opack
+    w = workloads.decode_point()
+    lat, rope, slots = w.all_written()
+    cache = np.zeros((w.num_pages + 1, 64, 352), dtype=np.uint8)
+    opack.pack_into_cache(lat.double().numpy(), rope.double().numpy(), slots.numpy(), cache)
+    call = lambda: oatt.sparse_mla_decode(w.q_latent, w.q_rope, cache, w.block_table, w.topk_idx, w.sm_scale,
+                                          w.q_seq_idx, w.seq_lens)
+    for _ in range(args.warmup):
+        call()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        call()
+        times.append(time.perf_counter() - t0)
+    v = statistics.mean(times) * 1e6
+    threads = blas_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": v / 1e3, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC, "T": w.T, "H": w.H, "topk": w.topk, "ctx": int(w.seq_lens[0]),
+                   "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"each step one whole decode call (15 tokens x 2048 slots), numpy float64, "
+                                   f"{threads}-thread BLAS on {os.cpu_count()} host cores"},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import numpy as np
+    import torch
+    import nvfp4_sparse_mla_gb300 as nvmla
+    from nvfp4_sparse_mla_gb300 import workloads
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    nvmla.load()
+    impl = {"auto": None, "mma": nvmla.IMPL_MMA, "tcgen05": nvmla.IMPL_TCGEN05}[args.kernel]
+
+    # ---------------- workload resident in HBM (replica per rank)
+    w = workloads.decode_point()
+    alg = algorithmic(w)
+    new_pages = 1
+    cache = torch.zeros((w.num_pages + new_pages, 64, 352), dtype=torch.uint8, device=dev)
+    lat, rope, slots = w.all_written()
+    nvmla.nvfp4_mla_pack(lat.to(dev), rope.to(dev), slots.to(dev), cache)
+    g = torch.Generator().manual_seed(77)
+    new_lat = torch.randn((w.T, 512), generator=g).to(torch.bfloat16)
+    new_rope = torch.randn((w.T, 64), generator=g).to(torch.bfloat16)
+    new_slots = torch.arange(w.num_pages * 64, w.num_pages * 64 + w.T, dtype=torch.int32)
+    d_new_lat, d_new_rope, d_new_slots = new_lat.to(dev), new_rope.to(dev), new_slots.to(dev)
+    ql, qr = w.q_latent.to(dev), w.q_rope.to(dev)
+    bt, tk = w.block_table.to(dev), w.topk_idx.to(dev)
+    qs, sl = w.q_seq_idx.to(dev), w.seq_lens.to(dev)
+    out = torch.empty((w.T, w.H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.T, w.H), dtype=torch.float32, device=dev)
+    ws_bytes = nvmla.sparse_mla_decode_workspace_size(w.T, w.H, w.topk, impl=impl)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def decode():
+        nvmla.sparse_mla_decode(ql, qr, cache, bt, tk, w.sm_scale, out=out, lse=lse, q_seq_idx=qs, seq_lens=sl,
+                                workspace=ws, impl=impl)
+
+    def pack_new():
+        nvmla.nvfp4_mla_pack(d_new_lat, d_new_rope, d_new_slots, cache)
+
+    for _ in range(max(3, args.warmup)):
+        flush.fill_(1.0)
+        pack_new()
+        decode()
+    torch.cuda.synchronize()
+
+    # ---------------- timed region
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    sampler = ClockSampler(local) if rank == 0 else None
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    launches0 = nvmla.launch_count()
+    t_wall0 = time.perf_counter()
+    for k in range(K):
+        flush.fill_(float(k))
+        ev[k][0].record()
+        pack_new()
+        ev[k][1].record()
+        decode()
+        ev[k][2].record()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    launches = nvmla.launch_count() - launches0
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop() if sampler else None
+    step_ms = [ev[k][0].elapsed_time(ev[k][2]) for k in range(K)]
+    dec_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)]
+    pack_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
+    dec_us = statistics.mean(dec_ms) * 1e3
+    step_mean = statistics.mean(step_ms)
+    if world > 1:
+        t = torch.tensor([dec_us, step_mean], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        dec_us, step_mean = float(t[0]), float(t[1])
+
+    # ---------------- end to end through the public API with host buffers
+    h_ql = w.q_latent.pin_memory()
+    h_qr = w.q_rope.pin_memory()
+    h_tk = w.topk_idx.pin_memory()
+    h_nl, h_nr, h_ns = new_lat.pin_memory(), new_rope.pin_memory(), new_slots.pin_memory()
+    h_out = torch.empty((w.T, w.H, 512), dtype=torch.bfloat16).pin_memory()
+    h_lse = torch.empty((w.T, w.H), dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_ql, h_qr, h_tk, h_nl, h_nr, h_ns))
+    d2h = h_out.numel() * 2 + h_lse.numel() * 4
+
+    def e2e_step():
+        d_ql = h_ql.to(dev, non_blocking=True)
+        d_qr = h_qr.to(dev, non_blocking=True)
+        d_tk = h_tk.to(dev, non_blocking=True)
+        d_nl, d_nr, d_ns = (h_nl.to(dev, non_blocking=True), h_nr.to(dev, non_blocking=True),
+                            h_ns.to(dev, non_blocking=True))
+        nvmla.nvfp4_mla_pack(d_nl, d_nr, d_ns, cache)
+        o, l = nvmla.sparse_mla_decode(d_ql, d_qr, cache, bt, d_tk, w.sm_scale, q_seq_idx=qs, seq_lens=sl,
+                                       workspace=ws, impl=impl)
+        h_out.copy_(o, non_blocking=True)
+        h_lse.copy_(l, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for k in range(K):
+        flush.fill_(float(k))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        e2e_step()
+        b.record()
+        b.synchronize()
+        e2e_ms.append(a.elapsed_time(b))
+    e2e_us = statistics.mean(e2e_ms) * 1e3
+
+    # ---------------- staged baseline (same workload, same protocol)
+    staged = None
+    if not args.no_staged:
+        buf = torch.empty((w.T, w.topk, 576), dtype=torch.uint8, device=dev)
+        ridx = torch.empty((w.T, w.topk), dtype=torch.int32, device=dev)
+        ws2 = nvmla.sparse_mla_decode_workspace_size(w.T, w.H, w.topk, impl=impl)
+        ws2 = torch.empty(max(ws2, 16), dtype=torch.uint8, device=dev)
+
+        def staged_call():
+            nvmla.nvfp4_stage_dequant_fp8(cache, bt, tk, qs, sl, fp8_rows=buf, row_idx=ridx)
+            nvmla.sparse_mla_decode_fp8rows(ql, qr, buf, ridx, w.sm_scale, out=out, lse=lse, workspace=ws2,
+                                            impl=impl)
+
+        for _ in range(3):
+            flush.fill_(1.0)
+            staged_call()
+        torch.cuda.synchronize()
+        sev = []
+        for k in range(K):
+            flush.fill_(float(k))
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            e[0].record()
+            nvmla.nvfp4_stage_dequant_fp8(cache, bt, tk, qs, sl, fp8_rows=buf, row_idx=ridx)
+            e[1].record()
+            nvmla.sparse_mla_decode_fp8rows(ql, qr, buf, ridx, w.sm_scale, out=out, lse=lse, workspace=ws2,
+                                            impl=impl)
+            e[2].record()
+            sev.append(e)
+        torch.cuda.synchronize()
+        s1 = [e[0].elapsed_time(e[1]) for e in sev]
+        s2 = [e[1].elapsed_time(e[2]) for e in sev]
+        staged = {"us_per_call": statistics.mean([a + b for a, b in zip(s1, s2)]) * 1e3,
+                  "dequant_us": statistics.mean(s1) * 1e3, "attend_us": statistics.mean(s2) * 1e3,
+                  "fp8_buffer_bytes": w.T * w.topk * 576}
+
+    # ---------------- pack of the write+read workload's 6144-token chunk
+    plat, prope, pslots = workloads.pack_chunk(seed=4, n=6144, num_pages=2188)
+    pcache = torch.zeros((2188, 64, 352), dtype=torch.uint8, device=dev)
+    plat, prope, pslots = plat.to(dev), prope.to(dev), pslots.to(dev)
+    for _ in range(3):
+        nvmla.nvfp4_mla_pack(plat, prope, pslots, pcache)
+    pk = []
+    for k in range(K):
+        flush.fill_(float(k))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        nvmla.nvfp4_mla_pack(plat, prope, pslots, pcache)
+        b.record()
+        pk.append(a)
+        pk.append(b)
+    torch.cuda.synchronize()
+    pack_us = statistics.mean([pk[2 * i].elapsed_time(pk[2 * i + 1]) for i in range(K)]) * 1e3
+    pack_bytes = 6144 * (1152 + 352 + 4)
+
+    if rank != 0:
+        return
+    pk_peaks, peak_src = peaks()
+    bw = pk_peaks["hbm_gbs"]
+    tf = pk_peaks["bf16_tflops"]
+    t_bytes = alg["bytes"] / (bw * 1e9) * 1e6
+    t_flops = alg["flops"] / (tf * 1e12) * 1e6
+    bound = "tensor" if t_flops >= t_bytes else "hbm"
+    if bound == "tensor":
+        achieved = alg["flops"] / (dec_us * 1e-6) / 1e12
+        peak, unit = tf, "TFLOP/s"
+    else:
+        achieved = alg["bytes"] / (dec_us * 1e-6) / 1e9
+        peak, unit = bw, "GB/s"
+    kernel_files = ["decode_tc.cu", "decode_mma.cu", "common.cuh"]
+    traffic = traffic_record(kernel_files, "decode_point")
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, args.cpu_seconds)
+    line = {
+        "metric": METRIC, "value": dec_us, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": step_mean, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16", "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC, "T": w.T, "H": w.H, "topk": w.topk, "ctx": int(w.seq_lens[0]),
+                   "valid_slots": alg["valid_slots"], "kernel": args.kernel,
+                   "l2": f"flushed before every step ({FLUSH_BYTES >> 20} MiB write)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+                     "peak_source": f"{peak_src} ({'bf16 burst; fp16 nominal rate equals bf16' if bound == 'tensor' else 'HBM copy'})",
+                     "roofline_us": max(t_bytes, t_flops), "bytes_us": t_bytes, "flops_us": t_flops,
+                     "algorithmic_bytes": alg["bytes"], "algorithmic_flops": alg["flops"],
+                     "effective_hbm_gbs": alg["bytes"] / (dec_us * 1e-6) / 1e9,
+                     "traffic": traffic},
+        "decode_us": {"mean": dec_us, "median": statistics.median(dec_ms) * 1e3, "min": min(dec_ms) * 1e3},
+        "pack_step_us": statistics.mean(pack_ms) * 1e3,
+        "pack_chunk": {"tokens": 6144, "us_per_call": pack_us, "gbs": pack_bytes / (pack_us * 1e-6) / 1e9,
+                       "frac_hbm": pack_bytes / (pack_us * 1e-6) / 1e9 / bw},
+        "staged": staged,
+        "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+        "wall_s_timed_region": t_wall,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

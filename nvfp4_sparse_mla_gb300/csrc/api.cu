@@ -24,8 +24,11 @@ size_t mma_workspace_bytes(int T, int H, int splits);
 
 // tcgen05 path (decode_tc.cu)
 bool tc_supported(int H);
+bool tc_fp8_rows_supported(int H);
+int tc_default_splits(int T, int H, int topk, int num_sms);
+size_t tc_workspace_bytes(int T, int H, int splits);
 cudaError_t launch_decode_tc(int fmt, const void*, const void*, const uint8_t*, const RowSelect&, const int32_t*,
-                             int, int, int, float, void*, float*, int32_t*, cudaStream_t);
+                             int, int, int, float, void*, float*, void*, int, int32_t*, cudaStream_t);
 
 namespace {
 
@@ -110,20 +113,39 @@ int pick_impl(const nvmla_decode_options* opts, int H) {
   return tc_supported(H) ? NVMLA_IMPL_TCGEN05 : NVMLA_IMPL_MMA;
 }
 
+bool tc_fp8_supported(int H) { return tc_fp8_rows_supported(H); }
+
+int pick_impl_fp8(const nvmla_decode_options* opts, int H) {
+  const int want = opts ? opts->impl : NVMLA_IMPL_AUTO;
+  if (want == NVMLA_IMPL_MMA) return NVMLA_IMPL_MMA;
+  if (want == NVMLA_IMPL_TCGEN05) return NVMLA_IMPL_TCGEN05;
+  return tc_fp8_supported(H) ? NVMLA_IMPL_TCGEN05 : NVMLA_IMPL_MMA;
+}
+
 // Split count for the mma kernel that fits the workspace (explicit requests
 // must fit; the heuristic falls back to fewer splits).
-nvmla_status pick_splits(const nvmla_decode_options* opts, int T, int H, int topk, size_t ws_bytes, const void* ws,
-                         int* splits) {
-  const int tiles = (topk + 63) / 64;
-  int s = (opts && opts->num_splits > 0) ? opts->num_splits : mma_default_splits(T, H, topk, num_sms());
+int impl_tile(int impl) { return impl == NVMLA_IMPL_TCGEN05 ? 128 : 64; }
+
+int default_splits(int impl, int T, int H, int topk) {
+  return impl == NVMLA_IMPL_TCGEN05 ? tc_default_splits(T, H, topk, num_sms()) : mma_default_splits(T, H, topk, num_sms());
+}
+
+size_t workspace_bytes(int impl, int T, int H, int splits) {
+  return impl == NVMLA_IMPL_TCGEN05 ? tc_workspace_bytes(T, H, splits) : mma_workspace_bytes(T, H, splits);
+}
+
+nvmla_status pick_splits(int impl, const nvmla_decode_options* opts, int T, int H, int topk, size_t ws_bytes,
+                         const void* ws, int* splits) {
+  const int tiles = (topk + impl_tile(impl) - 1) / impl_tile(impl);
+  int s = (opts && opts->num_splits > 0) ? opts->num_splits : default_splits(impl, T, H, topk);
   if (s > tiles) s = tiles;
   if (s < 1) s = 1;
   const bool explicit_req = opts && opts->num_splits > 0;
-  if (s > 1 && (!ws || mma_workspace_bytes(T, H, s) > ws_bytes)) {
+  if (s > 1 && (!ws || workspace_bytes(impl, T, H, s) > ws_bytes)) {
     if (explicit_req)
       return fail(NVMLA_ERR_WORKSPACE, "num_splits = %d needs %zu workspace bytes, got %zu", s,
-                  mma_workspace_bytes(T, H, s), ws ? ws_bytes : size_t(0));
-    while (s > 1 && (!ws || mma_workspace_bytes(T, H, s) > ws_bytes)) --s;
+                  workspace_bytes(impl, T, H, s), ws ? ws_bytes : size_t(0));
+    while (s > 1 && (!ws || workspace_bytes(impl, T, H, s) > ws_bytes)) --s;
   }
   if (ws && !aligned(ws, 16)) return fail(NVMLA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
   *splits = s;
@@ -176,11 +198,13 @@ nvmla_status nvfp4_mla_pack(const void* latent_bf16, int64_t latent_stride, cons
 
 size_t sparse_mla_decode_workspace_size_ex(int32_t T, int32_t H, int32_t topk, const nvmla_decode_options* opts) {
   if (T <= 0 || H <= 0 || H % 16 != 0 || H > NVMLA_MAX_HEADS || topk < 1 || topk > NVMLA_MAX_TOPK) return 0;
-  if (pick_impl(opts, H) == NVMLA_IMPL_TCGEN05) return 0;
-  const int tiles = (topk + 63) / 64;
-  int s = (opts && opts->num_splits > 0) ? opts->num_splits : mma_default_splits(T, H, topk, num_sms());
+  const int impl = pick_impl(opts, H);
+  if (impl == NVMLA_IMPL_TCGEN05 && !tc_supported(H)) return 0;
+  const int tiles = (topk + impl_tile(impl) - 1) / impl_tile(impl);
+  int s = (opts && opts->num_splits > 0) ? opts->num_splits : default_splits(impl, T, H, topk);
   if (s > tiles) s = tiles;
-  return mma_workspace_bytes(T, H, s);
+  if (s < 1) s = 1;
+  return workspace_bytes(impl, T, H, s);
 }
 
 size_t sparse_mla_decode_workspace_size(int32_t T, int32_t H, int32_t topk) {
@@ -188,7 +212,14 @@ size_t sparse_mla_decode_workspace_size(int32_t T, int32_t H, int32_t topk) {
 }
 
 size_t sparse_mla_decode_fp8rows_workspace_size(int32_t T, int32_t H, int32_t topk, const nvmla_decode_options* opts) {
-  return sparse_mla_decode_workspace_size_ex(T, H, topk, opts);
+  if (T <= 0 || H <= 0 || H % 16 != 0 || H > NVMLA_MAX_HEADS || topk < 1 || topk > NVMLA_MAX_TOPK) return 0;
+  const int impl = pick_impl_fp8(opts, H);
+  if (impl == NVMLA_IMPL_TCGEN05 && !tc_fp8_supported(H)) return 0;
+  const int tiles = (topk + impl_tile(impl) - 1) / impl_tile(impl);
+  int s = (opts && opts->num_splits > 0) ? opts->num_splits : default_splits(impl, T, H, topk);
+  if (s > tiles) s = tiles;
+  if (s < 1) s = 1;
+  return workspace_bytes(impl, T, H, s);
 }
 
 nvmla_status sparse_mla_decode_ex(const void* q_latent, const void* q_rope, const uint8_t* cache, int64_t num_pages,
@@ -207,14 +238,15 @@ nvmla_status sparse_mla_decode_ex(const void* q_latent, const void* q_rope, cons
   RowSelect sel{topk_idx, block_table, q_seq_idx, seq_lens, num_pages * NVMLA_PAGE_TOKENS, topk, max_pages_per_seq};
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int impl = pick_impl(opts, H);
-  if (impl == NVMLA_IMPL_TCGEN05) {
-    if (!tc_supported(H)) return fail(NVMLA_ERR_UNSUPPORTED, "the tcgen05 kernel needs H a multiple of 64 (H = %d)", H);
-    return counted(launch_decode_tc(0, q_latent, q_rope, cache, sel, nullptr, T, H, topk, sm_scale, out, lse,
-                                    err_word, st),
-                   1, "sparse_mla_decode (tcgen05) launch");
-  }
+  if (impl == NVMLA_IMPL_TCGEN05 && !tc_supported(H))
+    return fail(NVMLA_ERR_UNSUPPORTED, "the tcgen05 kernel needs H a multiple of 64 (H = %d)", H);
   int splits = 1;
-  if ((s = pick_splits(opts, T, H, topk, workspace_bytes, workspace, &splits)) != NVMLA_OK) return s;
+  if ((s = pick_splits(impl, opts, T, H, topk, workspace_bytes, workspace, &splits)) != NVMLA_OK) return s;
+  if (impl == NVMLA_IMPL_TCGEN05) {
+    return counted(launch_decode_tc(0, q_latent, q_rope, cache, sel, nullptr, T, H, topk, sm_scale, out, lse,
+                                    workspace, splits, err_word, st),
+                   splits > 1 ? 2 : 1, "sparse_mla_decode (tcgen05) launch");
+  }
   return counted(launch_decode_mma(0, q_latent, q_rope, cache, sel, nullptr, T, H, topk, sm_scale, out, lse,
                                    workspace, splits, err_word, st),
                  splits > 1 ? 2 : 1, "sparse_mla_decode (mma) launch");
@@ -261,15 +293,16 @@ nvmla_status sparse_mla_decode_fp8rows(const void* q_latent, const void* q_rope,
     return fail(NVMLA_ERR_INVALID_ARG, "bad options");
   RowSelect sel{};
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const int impl = pick_impl(opts, H);
-  if (impl == NVMLA_IMPL_TCGEN05) {
-    if (!tc_supported(H)) return fail(NVMLA_ERR_UNSUPPORTED, "the tcgen05 kernel needs H a multiple of 64 (H = %d)", H);
-    return counted(launch_decode_tc(1, q_latent, q_rope, fp8_rows, sel, row_idx, T, H, topk, sm_scale, out, lse,
-                                    err_word, st),
-                   1, "sparse_mla_decode_fp8rows (tcgen05) launch");
-  }
+  const int impl = pick_impl_fp8(opts, H);
+  if (impl == NVMLA_IMPL_TCGEN05 && !tc_fp8_supported(H))
+    return fail(NVMLA_ERR_UNSUPPORTED, "no tcgen05 kernel for FP8 rows with H = %d", H);
   int splits = 1;
-  if ((s = pick_splits(opts, T, H, topk, workspace_bytes, workspace, &splits)) != NVMLA_OK) return s;
+  if ((s = pick_splits(impl, opts, T, H, topk, workspace_bytes, workspace, &splits)) != NVMLA_OK) return s;
+  if (impl == NVMLA_IMPL_TCGEN05) {
+    return counted(launch_decode_tc(1, q_latent, q_rope, fp8_rows, sel, row_idx, T, H, topk, sm_scale, out, lse,
+                                    workspace, splits, err_word, st),
+                   splits > 1 ? 2 : 1, "sparse_mla_decode_fp8rows (tcgen05) launch");
+  }
   return counted(launch_decode_mma(1, q_latent, q_rope, fp8_rows, sel, row_idx, T, H, topk, sm_scale, out, lse,
                                    workspace, splits, err_word, st),
                  splits > 1 ? 2 : 1, "sparse_mla_decode_fp8rows (mma) launch");

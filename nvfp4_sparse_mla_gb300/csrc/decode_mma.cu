@@ -365,6 +365,12 @@ __global__ void __launch_bounds__(128) merge_splits_kernel(const float* __restri
   if (threadIdx.x == 0) lse[th] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
 }
 
+cudaError_t launch_merge(const float* ws_o, const float* ws_ml, int T, int S, int H, __nv_bfloat16* out, float* lse,
+                         cudaStream_t stream) {
+  merge_splits_kernel<<<T * H, 128, 0, stream>>>(ws_o, ws_ml, S, H, out, lse);
+  return cudaGetLastError();
+}
+
 size_t mma_smem_bytes(int fmt, int topk_per_cta) {
   const int raw = fmt == kNvfp4Paged ? kRowBytes : kFp8RowBytes;
   return static_cast<size_t>(2 * 64 * kRowB) + 2 * kKT * raw + sizeof(int32_t) * ((topk_per_cta + 63) / 64 * 64);
@@ -422,8 +428,7 @@ cudaError_t launch_decode_mma(int fmt, const void* q_latent, const void* q_rope,
   }
   e = cudaGetLastError();
   if (e != cudaSuccess || splits == 1) return e;
-  merge_splits_kernel<<<T * H, 128, 0, stream>>>(p.ws_o, p.ws_ml, splits, H, p.out, lse);
-  return cudaGetLastError();
+  return launch_merge(p.ws_o, p.ws_ml, T, splits, H, p.out, lse, stream);
 }
 
 }  // namespace nvmla

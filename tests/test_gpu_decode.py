@@ -15,11 +15,16 @@ from nvfp4_sparse_mla_gb300 import workloads
 
 pytestmark = pytest.mark.gpu
 
-IMPLS = ["auto", "mma"]
+IMPLS = ["auto", "mma", "tcgen05"]
 
 
 def _impl(lib, name):
     return {"auto": None, "mma": lib.IMPL_MMA, "tcgen05": lib.IMPL_TCGEN05}[name]
+
+
+def _skip_unsupported(impl, H):
+    if impl == "tcgen05" and H % 64 != 0:
+        pytest.skip("the tcgen05 kernel covers head counts that are multiples of 64")
 
 
 @pytest.fixture(scope="module")
@@ -43,6 +48,7 @@ def run(lib, w, cache, dev, impl=None, num_splits=None, **over):
 @pytest.mark.parametrize("splits", [None, 1, 3, 4])
 def test_tiny(lib, cuda, tiny_setup, impl, splits):
     w, cache, ref_cache = tiny_setup
+    _skip_unsupported(impl, w.H)
     ro, rl, _ = parity.oracle_decode(w, ref_cache)
     out, lse = run(lib, w, cache, cuda, impl=_impl(lib, impl), num_splits=splits)
     parity.assert_close(out, lse, ro, rl, f"tiny/{impl}/{splits}")
@@ -93,6 +99,7 @@ def _small(seed, T=3, H=64, ctx=1000, topk=300, pad=0.2):
 @pytest.mark.parametrize("topk", [1, 17, 64, 100, 300])
 @pytest.mark.parametrize("impl", IMPLS)
 def test_shapes(lib, cuda, H, topk, impl):
+    _skip_unsupported(impl, H)
     w = workloads.padded(seed=100 + H + topk, T=3, H=H, ctx=700, topk=topk, max_pad_frac=0.3)
     cache = parity.device_cache(lib, w, cuda)
     ref_cache = parity.oracle_cache(w)
@@ -104,6 +111,7 @@ def test_shapes(lib, cuda, H, topk, impl):
 @pytest.mark.parametrize("impl", IMPLS)
 def test_all_padding(lib, cuda, tiny_setup, impl):
     w, cache, _ = tiny_setup
+    _skip_unsupported(impl, w.H)
     pad = torch.full_like(w.topk_idx, -1).to(cuda)
     out, lse = run(lib, w, cache, cuda, impl=_impl(lib, impl), topk_idx=pad)
     assert torch.all(out == 0) and torch.all(torch.isneginf(lse))
@@ -180,3 +188,46 @@ def test_small_workspace_falls_back(lib, cuda, tiny_setup):
     out, lse = lib.sparse_mla_decode(d["q_latent"], d["q_rope"], cache, d["block_table"], d["topk_idx"], w.sm_scale,
                                      workspace=ws, impl=lib.IMPL_MMA)
     parity.assert_close(out, lse, ro, rl, "fallback")
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 16])
+def test_tcgen05_splits(lib, cuda, splits):
+    """The tcgen05 kernel with explicit key splits (single CTA per token up to
+    one CTA per 128-row tile), on the decode-point shape with fewer tokens."""
+    w = workloads.decode_point(seed=11, T=3, ctx=50_000)
+    cache = parity.device_cache(lib, w, cuda)
+    ref_cache = parity.oracle_cache(w)
+    ro, rl, _ = parity.oracle_decode(w, ref_cache)
+    err = torch.zeros(2, dtype=torch.int32, device=cuda)
+    d = parity.device_inputs(w, cuda)
+    out, lse = lib.sparse_mla_decode(d["q_latent"], d["q_rope"], cache, d["block_table"], d["topk_idx"], w.sm_scale,
+                                     q_seq_idx=d["q_seq_idx"], seq_lens=d["seq_lens"], err_word=err,
+                                     impl=lib.IMPL_TCGEN05, num_splits=splits)
+    parity.assert_close(out, lse, ro, rl, f"tcgen05 splits={splits}")
+    assert err.cpu().tolist() == [0, 0]
+
+
+def test_tcgen05_rejects_other_head_counts(lib, cuda, tiny_setup):
+    w, cache, _ = tiny_setup
+    d = parity.device_inputs(w, cuda)
+    with pytest.raises(lib.NvmlaError):
+        lib.sparse_mla_decode(d["q_latent"], d["q_rope"], cache, d["block_table"], d["topk_idx"], w.sm_scale,
+                              impl=lib.IMPL_TCGEN05)
+
+
+def test_large_score_range_rescales(lib, cuda):
+    """Scores spread over a wide range (queries scaled x8) force the running
+    maximum up across tiles, exercising the rescale of the accumulator."""
+    w = workloads.decode_point(seed=12, T=2, ctx=20_000)
+    w.q_latent = (w.q_latent.float() * 8).to(torch.bfloat16)
+    w.q_rope = (w.q_rope.float() * 8).to(torch.bfloat16)
+    cache = parity.device_cache(lib, w, cuda)
+    ref_cache = parity.oracle_cache(w)
+    ro, rl, _ = parity.oracle_decode(w, ref_cache)
+    for impl in (lib.IMPL_MMA, lib.IMPL_TCGEN05):
+        for splits in (1, 2):
+            d = parity.device_inputs(w, cuda)
+            out, lse = lib.sparse_mla_decode(d["q_latent"], d["q_rope"], cache, d["block_table"], d["topk_idx"],
+                                             w.sm_scale, q_seq_idx=d["q_seq_idx"], seq_lens=d["seq_lens"],
+                                             impl=impl, num_splits=splits)
+            parity.assert_close(out, lse, ro, rl, f"wide scores impl={impl} splits={splits}")
