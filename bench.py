@@ -32,6 +32,8 @@ sys.path.insert(0, ROOT)
 METRIC = "sparse-MLA NVFP4 decode µs/call & % roofline (15 q-tok × top-2048, 1 GB300)"
 UNIT = "us/call"
 FLUSH_BYTES = 256 << 20
+GROUP = 16                       # steps enqueued behind one GPU sleep
+LEAD_CYCLES_PER_STEP = 400_000   # ~0.2 ms of sleep per queued step
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 WORKLOAD_DESC = ("decode_point: 15 query tokens (1 sequence) x top-2048 distinct uniform positions, 64 heads, "
                  "200K-token context, 64-token pages, NVFP4 latent 512 + FP8 RoPE 64 (352 B/row)")
@@ -40,7 +42,7 @@ WORKLOAD_DESC = ("decode_point: 15 query tokens (1 sequence) x top-2048 distinct
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--kernel", default="auto", choices=["auto", "mma", "tcgen05"])
@@ -82,50 +84,67 @@ def algorithmic(w):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling during the timed region."""
+    """nvidia-smi clock and throttle-reason samples (every 20 ms) taken in the
+    background; stop() keeps the samples that fall inside a wall-clock window
+    around the timed region."""
+
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, gpu_index: int):
         self.proc = None
         self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
-        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+        q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
         try:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={q}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
 
-    def stop(self):
+    @staticmethod
+    def _ts(text):
+        import datetime
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.datetime.strptime(text.strip(), fmt).timestamp()
+            except ValueError:
+                pass
+        return None
+
+    def stop(self, t0: float, t1: float, pad: float = 0.05):
         if self.proc is None:
             return None
+        time.sleep(0.1)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
         self.f.close()
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
         for line in open(self.path):
             parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
+                rows.append((self._ts(parts[0]), float(parts[2]), float(parts[3]), float(parts[4]), parts[6:10]))
             except ValueError:
                 continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        if not sm:
+        if not rows:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
-                "reasons": sorted(reasons)}
+        inside = [r for r in rows if r[0] is not None and t0 - pad <= r[0] <= t1 + pad]
+        window = "timed region +-50 ms"
+        if not inside:
+            inside = sorted(rows, key=lambda r: abs((r[0] or t0) - (t0 + t1) / 2))[:3]
+            window = "3 samples nearest the timed region"
+        reasons = sorted({n for r in inside for n, v in zip(self.NAMES, r[4]) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "power_w_max": max(r[3] for r in inside), "samples": len(inside), "window": window,
+                "reasons": reasons}
 
 
 def source_hash(names):
@@ -136,16 +155,21 @@ def source_hash(names):
     return h.hexdigest()[:16]
 
 
-def traffic_record(kernel_files, launch_key):
-    """DRAM traffic per launch from a committed ncu summary, or None when the
-    kernel source changed since the counters were taken."""
+KERNEL_FILES = {"decode_tc_kernel": ["decode_tc.cu", "common.cuh"],
+                "decode_mma_kernel": ["decode_mma.cu", "common.cuh"]}
+
+
+def traffic_record(kernel):
+    """DRAM bytes per launch of `kernel` on this workload from the committed
+    ncu summary (profiles/traffic.json), or None when the kernel's source
+    changed since the counters were taken."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
-    rec = d.get(launch_key)
-    if not rec or rec.get("source_hash") != source_hash(kernel_files):
+    rec = d.get(kernel)
+    if not rec or rec.get("source_hash") != source_hash(KERNEL_FILES[kernel]):
         return None
     return rec.get("dram_bytes_per_launch")
 
@@ -283,15 +307,23 @@ def main():
     torch.cuda.synchronize()
 
     # ---------------- timed region
+    # Steps are enqueued in groups behind a GPU sleep, so that the host has
+    # queued a whole group before the GPU reaches it: the events of a step
+    # then bracket device work only, never host enqueue time. The sleeps,
+    # like the L2 flushes, sit between steps.
     K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     sampler = ClockSampler(local) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0.0)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     launches0 = nvmla.launch_count()
     t_wall0 = time.perf_counter()
+    t_epoch0 = time.time()
     for k in range(K):
+        if k % GROUP == 0:
+            torch.cuda._sleep(LEAD_CYCLES_PER_STEP * min(GROUP, K - k))
         flush.fill_(float(k))
         ev[k][0].record()
         pack_new()
@@ -300,10 +332,11 @@ def main():
         ev[k][2].record()
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall0
+    t_epoch1 = time.time()
     launches = nvmla.launch_count() - launches0
     if world > 1:
         torch.distributed.barrier()
-    clocks = sampler.stop() if sampler else None
+    clocks = sampler.stop(t_epoch0, t_epoch1) if sampler else None
     step_ms = [ev[k][0].elapsed_time(ev[k][2]) for k in range(K)]
     dec_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)]
     pack_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
@@ -355,7 +388,7 @@ def main():
     if not args.no_staged:
         buf = torch.empty((w.T, w.topk, 576), dtype=torch.uint8, device=dev)
         ridx = torch.empty((w.T, w.topk), dtype=torch.int32, device=dev)
-        ws2 = nvmla.sparse_mla_decode_workspace_size(w.T, w.H, w.topk, impl=impl)
+        ws2 = nvmla.sparse_mla_decode_fp8rows_workspace_size(w.T, w.H, w.topk, impl=impl)
         ws2 = torch.empty(max(ws2, 16), dtype=torch.uint8, device=dev)
 
         def staged_call():
@@ -369,6 +402,8 @@ def main():
         torch.cuda.synchronize()
         sev = []
         for k in range(K):
+            if k % GROUP == 0:
+                torch.cuda._sleep(LEAD_CYCLES_PER_STEP * min(GROUP, K - k))
             flush.fill_(float(k))
             e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
             e[0].record()
@@ -393,6 +428,8 @@ def main():
         nvmla.nvfp4_mla_pack(plat, prope, pslots, pcache)
     pk = []
     for k in range(K):
+        if k % GROUP == 0:
+            torch.cuda._sleep(LEAD_CYCLES_PER_STEP * min(GROUP, K - k))
         flush.fill_(float(k))
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
@@ -418,8 +455,8 @@ def main():
     else:
         achieved = alg["bytes"] / (dec_us * 1e-6) / 1e9
         peak, unit = bw, "GB/s"
-    kernel_files = ["decode_tc.cu", "decode_mma.cu", "common.cuh"]
-    traffic = traffic_record(kernel_files, "decode_point")
+    kernel = "decode_tc_kernel" if args.kernel in ("auto", "tcgen05") and w.H % 64 == 0 else "decode_mma_kernel"
+    traffic = traffic_record(kernel)
     cpu = None
     if not args.no_cpu_baseline:
         cpu = cpu_baseline(w, args.cpu_seconds)
@@ -436,6 +473,7 @@ def main():
                      "roofline_us": max(t_bytes, t_flops), "bytes_us": t_bytes, "flops_us": t_flops,
                      "algorithmic_bytes": alg["bytes"], "algorithmic_flops": alg["flops"],
                      "effective_hbm_gbs": alg["bytes"] / (dec_us * 1e-6) / 1e9,
+                     "kernel": kernel, "timed": "whole decode call (CUDA events on the launching stream)",
                      "traffic": traffic},
         "decode_us": {"mean": dec_us, "median": statistics.median(dec_ms) * 1e3, "min": min(dec_ms) * 1e3},
         "pack_step_us": statistics.mean(pack_ms) * 1e3,

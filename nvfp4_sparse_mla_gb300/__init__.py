@@ -24,7 +24,7 @@ from typing import Optional
 import torch
 
 __all__ = [
-    "NvmlaError", "nvfp4_mla_pack", "sparse_mla_decode", "sparse_mla_decode_workspace_size", "launch_count",
+    "NvmlaError", "nvfp4_mla_pack", "sparse_mla_decode", "sparse_mla_decode_workspace_size", "sparse_mla_decode_fp8rows_workspace_size", "launch_count",
     "nvfp4_stage_dequant_fp8", "sparse_mla_decode_fp8rows", "library_path", "load",
     "IMPL_AUTO", "IMPL_MMA", "IMPL_TCGEN05", "ROW_BYTES", "FP8_ROW_BYTES", "PAGE_TOKENS",
 ]
@@ -158,6 +158,11 @@ def nvfp4_mla_pack(latent: torch.Tensor, rope: torch.Tensor, slot_mapping: torch
 def sparse_mla_decode_workspace_size(T: int, H: int, topk: int, impl=None, num_splits=None) -> int:
     lib = load()
     return int(lib.sparse_mla_decode_workspace_size_ex(T, H, topk, _opts(impl, num_splits)))
+
+
+def sparse_mla_decode_fp8rows_workspace_size(T: int, H: int, topk: int, impl=None, num_splits=None) -> int:
+    lib = load()
+    return int(lib.sparse_mla_decode_fp8rows_workspace_size(T, H, topk, _opts(impl, num_splits)))
 
 
 def sparse_mla_decode(q_latent: torch.Tensor, q_rope: torch.Tensor, cache: torch.Tensor, block_table: torch.Tensor,
