@@ -195,6 +195,43 @@ size_t sparse_mla_decode_workspace_size_ex(int32_t T, int32_t H, int32_t topk,
                                            const nvmla_decode_options* opts);
 
 /*
+ * sparse_mla_decode_noalloc -- sparse_mla_decode without a workspace
+ * argument. The pages describe no such call: it exists for callers that
+ * cannot allocate GPU memory (an engine whose memory pool owns the whole
+ * GPU, a replayed fixed launch sequence, a C caller with no allocator). The
+ * call allocates nothing: the split partials go to a scratch array of
+ * sparse_mla_decode_noalloc_max_scratch() bytes (16 MiB) in device memory
+ * owned by the library, reserved on each device where the library's code
+ * loads and held until the process exits.
+ *
+ *   Arguments, results and err_word: as sparse_mla_decode.
+ *   Same kernels and split count as sparse_mla_decode given a workspace of
+ *   sparse_mla_decode_workspace_size(T, H, topk) bytes, hence the same output
+ *   bits.
+ *   Returns NVMLA_ERR_WORKSPACE, launching nothing, when that size exceeds the
+ *   scratch (H a multiple of 64 always fits on GPUs with up to 254 SMs; some
+ *   other H at large T do not).
+ *   The first call on each device looks up the scratch's address
+ *   (cudaGetSymbolAddress); make it before any stream capture on that device.
+ *   The scratch is shared: calls whose work overlaps on the GPU (different
+ *   streams, threads or processes sharing one context) race on it and give
+ *   wrong results. Order such calls on one stream or by events.
+ *   Nothing needs zeroing beforehand; the scratch is not cleared afterwards.
+ */
+nvmla_status sparse_mla_decode_noalloc(const void* q_latent, const void* q_rope,
+                                       const uint8_t* cache, int64_t num_pages,
+                                       const int32_t* block_table, int32_t num_seqs,
+                                       int32_t max_pages_per_seq,
+                                       const int32_t* topk_idx, int32_t topk,
+                                       const int32_t* q_seq_idx, const int32_t* seq_lens,
+                                       int32_t T, int32_t H, float sm_scale,
+                                       void* out, float* lse,
+                                       int32_t* err_word, nvmla_stream_t stream);
+
+/* Bytes of scratch sparse_mla_decode_noalloc holds per device. */
+size_t sparse_mla_decode_noalloc_max_scratch(void);
+
+/*
  * nvfp4_stage_dequant_fp8 -- stage 1 of the staged baseline [KV, "KV 캐시와
  * 데이터 전송": the compressed rows were first unpacked into a temporary FP8
  * buffer in GPU memory; 4-bit, section text before items 1-3].

@@ -11,6 +11,8 @@ Calls (same names as the C ABI, see include/nvmla.h):
 
 * ``nvfp4_mla_pack(latent, rope, slot_mapping, cache)``
 * ``sparse_mla_decode(q_latent, q_rope, cache, block_table, topk_idx, sm_scale, ...)``
+* ``sparse_mla_decode_noalloc(q_latent, q_rope, cache, block_table, topk_idx, sm_scale, out, lse, ...)``
+  (the same decode with the library's own split scratch; allocates nothing)
 * ``nvfp4_stage_dequant_fp8(cache, block_table, topk_idx, ...)`` and
   ``sparse_mla_decode_fp8rows(q_latent, q_rope, fp8_rows, row_idx, sm_scale, ...)``
   (the staged baseline)
@@ -26,6 +28,7 @@ import torch
 __all__ = [
     "NvmlaError", "nvfp4_mla_pack", "sparse_mla_decode", "sparse_mla_decode_workspace_size", "sparse_mla_decode_fp8rows_workspace_size", "launch_count",
     "nvfp4_stage_dequant_fp8", "sparse_mla_decode_fp8rows", "library_path", "load",
+    "sparse_mla_decode_noalloc", "sparse_mla_decode_noalloc_max_scratch",
     "IMPL_AUTO", "IMPL_MMA", "IMPL_TCGEN05", "ROW_BYTES", "FP8_ROW_BYTES", "PAGE_TOKENS",
 ]
 
@@ -73,6 +76,8 @@ def load():
         "sparse_mla_decode_ex": (I32, [P, P, P, I64, P, I32, I32, P, I32, P, P, I32, I32, F, P, P, P, SZ, P, OPT, P]),
         "sparse_mla_decode_workspace_size": (SZ, [I32, I32, I32]),
         "sparse_mla_decode_workspace_size_ex": (SZ, [I32, I32, I32, OPT]),
+        "sparse_mla_decode_noalloc": (I32, [P, P, P, I64, P, I32, I32, P, I32, P, P, I32, I32, F, P, P, P, P]),
+        "sparse_mla_decode_noalloc_max_scratch": (SZ, []),
         "nvfp4_stage_dequant_fp8": (I32, [P, I64, P, I32, I32, P, I32, P, P, I32, P, P, P, P]),
         "sparse_mla_decode_fp8rows": (I32, [P, P, P, P, I32, I32, I32, F, P, P, P, SZ, P, OPT, P]),
         "sparse_mla_decode_fp8rows_workspace_size": (SZ, [I32, I32, I32, OPT]),
@@ -206,6 +211,49 @@ def sparse_mla_decode(q_latent: torch.Tensor, q_rope: torch.Tensor, cache: torch
                                     block_table.shape[0], block_table.shape[1], _ptr(topk_idx), topk,
                                     _ptr(q_seq_idx), _ptr(seq_lens), T, H, float(sm_scale), _ptr(out), _ptr(lse),
                                     _ptr(workspace), ws_bytes, _ptr(err_word), opts, _stream(q_latent, stream)))
+    return out, lse
+
+
+def sparse_mla_decode_noalloc_max_scratch() -> int:
+    """Bytes of split scratch the library holds per device for
+    sparse_mla_decode_noalloc."""
+    return int(load().sparse_mla_decode_noalloc_max_scratch())
+
+
+def sparse_mla_decode_noalloc(q_latent: torch.Tensor, q_rope: torch.Tensor, cache: torch.Tensor,
+                              block_table: torch.Tensor, topk_idx: torch.Tensor, sm_scale: float,
+                              out: torch.Tensor, lse: torch.Tensor, q_seq_idx: Optional[torch.Tensor] = None,
+                              seq_lens: Optional[torch.Tensor] = None, err_word: Optional[torch.Tensor] = None,
+                              stream=None):
+    """sparse_mla_decode for callers that cannot allocate: out (bf16
+    [T,H,512]) and lse (fp32 [T,H]) are required, the split partials go to the
+    library's own scratch, and neither this function nor the library
+    allocates GPU memory. Calls that overlap on the GPU share that scratch
+    and race. Returns (out, lse)."""
+    _need(q_latent, "q_latent", torch.bfloat16, 3)
+    _need(q_rope, "q_rope", torch.bfloat16, 3)
+    _need(cache, "cache", torch.uint8, 3)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(topk_idx, "topk_idx", torch.int32, 2)
+    _need(out, "out", torch.bfloat16, 3)
+    _need(lse, "lse", torch.float32, 2)
+    T, H, dl = q_latent.shape
+    if dl != 512 or tuple(q_rope.shape) != (T, H, 64):
+        raise ValueError("q_latent must be [T, H, 512] and q_rope [T, H, 64]")
+    if topk_idx.shape[0] != T or tuple(out.shape) != (T, H, 512) or tuple(lse.shape) != (T, H):
+        raise ValueError("topk_idx must be [T, topk], out [T, H, 512] and lse [T, H]")
+    if cache.shape[1:] != (PAGE_TOKENS, ROW_BYTES):
+        raise ValueError("cache must be [num_pages, 64, 352]")
+    if q_seq_idx is not None:
+        _need(q_seq_idx, "q_seq_idx", torch.int32, 1)
+    if seq_lens is not None:
+        _need(seq_lens, "seq_lens", torch.int32, 1)
+    lib = load()
+    _check(lib.sparse_mla_decode_noalloc(_ptr(q_latent), _ptr(q_rope), _ptr(cache), cache.shape[0],
+                                         _ptr(block_table), block_table.shape[0], block_table.shape[1],
+                                         _ptr(topk_idx), topk_idx.shape[1], _ptr(q_seq_idx), _ptr(seq_lens), T, H,
+                                         float(sm_scale), _ptr(out), _ptr(lse), _ptr(err_word),
+                                         _stream(q_latent, stream)))
     return out, lse
 
 

@@ -153,6 +153,11 @@ nvmla_status pick_splits(int impl, const nvmla_decode_options* opts, int T, int 
 }
 
 }  // namespace
+
+// Records `msg` as the calling thread's last error and returns `s` (for the
+// entry points defined in other translation units).
+nvmla_status record_error(nvmla_status s, const char* msg) { return fail(s, "%s", msg); }
+
 }  // namespace nvmla
 
 using namespace nvmla;
