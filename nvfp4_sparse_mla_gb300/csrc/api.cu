@@ -26,6 +26,7 @@ size_t mma_workspace_bytes(int T, int H, int splits);
 bool tc_supported(int H);
 bool tc_fp8_rows_supported(int H);
 int tc_default_splits(int T, int H, int topk, int num_sms);
+int tc_max_splits();
 size_t tc_workspace_bytes(int T, int H, int splits);
 cudaError_t launch_decode_tc(int fmt, const void*, const void*, const uint8_t*, const RowSelect&, const int32_t*,
                              int, int, int, float, void*, float*, void*, int, int32_t*, cudaStream_t);
@@ -141,12 +142,19 @@ nvmla_status pick_splits(int impl, const nvmla_decode_options* opts, int T, int 
   if (s > tiles) s = tiles;
   if (s < 1) s = 1;
   const bool explicit_req = opts && opts->num_splits > 0;
-  if (s > 1 && (!ws || workspace_bytes(impl, T, H, s) > ws_bytes)) {
+  auto too_small = [&](int n) {
+    const size_t need = workspace_bytes(impl, T, H, n);
+    return need > 0 && (!ws || need > ws_bytes);
+  };
+  if (s > 1 && too_small(s)) {
     if (explicit_req)
       return fail(NVMLA_ERR_WORKSPACE, "num_splits = %d needs %zu workspace bytes, got %zu", s,
                   workspace_bytes(impl, T, H, s), ws ? ws_bytes : size_t(0));
-    while (s > 1 && (!ws || workspace_bytes(impl, T, H, s) > ws_bytes)) --s;
+    while (s > 1 && too_small(s)) --s;
   }
+  if (impl == NVMLA_IMPL_TCGEN05 && s > tc_max_splits())
+    return fail(NVMLA_ERR_UNSUPPORTED, "num_splits = %d exceeds the %d CTAs a cluster can hold on this device", s,
+                tc_max_splits());
   if (ws && !aligned(ws, 16)) return fail(NVMLA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
   *splits = s;
   return NVMLA_OK;
@@ -250,7 +258,7 @@ nvmla_status sparse_mla_decode_ex(const void* q_latent, const void* q_rope, cons
   if (impl == NVMLA_IMPL_TCGEN05) {
     return counted(launch_decode_tc(0, q_latent, q_rope, cache, sel, nullptr, T, H, topk, sm_scale, out, lse,
                                     workspace, splits, err_word, st),
-                   splits > 1 ? 2 : 1, "sparse_mla_decode (tcgen05) launch");
+                   1, "sparse_mla_decode (tcgen05) launch");
   }
   return counted(launch_decode_mma(0, q_latent, q_rope, cache, sel, nullptr, T, H, topk, sm_scale, out, lse,
                                    workspace, splits, err_word, st),

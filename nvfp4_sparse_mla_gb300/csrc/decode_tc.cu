@@ -4,19 +4,23 @@
 // Open Models", section "A native NVFP4 sparse-MLA decode kernel" -- for each
 // query token only the rows the indexer selected are loaded, unpacked on chip
 // and attended to with FP16 operands and FP32 accumulation, with no FP8
-// staging buffer in GPU memory. "Prime Intellect unveils Prime Inference",
-// section "4-bit caches open the way": item 1 (one warp group unpacks rows
-// while others compute scores and accumulate), item 3 (empty slots of the
-// 2048-slot list contribute nothing).
+// staging buffer in GPU memory; the token's selected rows are divided among a
+// cluster of cooperating CTAs whose partial results are combined through
+// distributed shared memory in the same launch. "Prime Intellect unveils
+// Prime Inference", section "4-bit caches open the way": item 1 (one warp
+// group unpacks rows while others compute scores and accumulate), item 3
+// (empty slots of the 2048-slot list contribute nothing).
 //
-// One CTA = one query token x 64 heads x a range of the token's slots, taken
-// in tiles of 128 rows. Roles:
+// One cluster = one query token x 64 heads; its S CTAs take contiguous
+// ranges of the token's slots, in tiles of 128 rows. Roles in a CTA:
 //
 //   warps 0-7  unpack: thread (row r, part h) loads the parts of its cache
-//              row it needs (192 of the 352 bytes) straight into registers,
-//              one tile ahead, and writes fp16 operands (E2M1 x E4M3 is exact
-//              in fp16) into shared memory, 128B-swizzled: latent chunk
-//              c = 2j + h (64 dims) for j = 0..3 and half of the RoPE chunk.
+//              row it needs (192 of the 352 bytes) straight into registers
+//              and writes fp16 operands (E2M1 x E4M3 is exact in fp16) into
+//              shared memory, 128B-swizzled: latent chunk c = 2j + h (64
+//              dims) for j = 0..3 and half of the RoPE chunk. Each piece of
+//              the next tile's row is requested as soon as the current tile
+//              no longer needs its registers.
 //   MMA issue: one softmax thread issues QK as chunk pairs land and PV as
 //              soon as P^T is written; M = 128 throughout:
 //                S^T[128 rows, 64 heads]   = K[128 x 576] . Q^T   (9 chunks)
@@ -25,22 +29,33 @@
 //              64-dim chunk is byte for byte the MN-major layout of V^T for
 //              those 64 value dims, so block j of PV reads chunks 2j, 2j+1.
 //              Block j's completion frees chunks 2j, 2j+1 for the next tile.
-//   warps 8-11 softmax: thread = row (TMEM lane). The running maximum of
-//              every head stays fixed while no score exceeds it by more than
-//              2^8 (P stays below 256, safe in fp16); only a tile that does
-//              (always the first) pays for the exact cross-row maximum and
-//              the rescale of O^T in TMEM. Row sums accumulate per thread and
-//              are reduced across rows once, at the end. P^T goes to shared
-//              memory in place of the RoPE chunk, which QK no longer needs.
+//   warps 8-15 softmax: warp (lane quadrant q, head half g) owns TMEM lanes
+//              32q..32q+31 (= rows) and heads 32g..32g+31. The running
+//              maximum of every head stays fixed while no score exceeds it by
+//              more than 2^8 (P stays below 256, safe in fp16); only a tile
+//              that does (always the first) pays for the exact cross-row
+//              maximum and the rescale of O^T in TMEM. Row sums accumulate per
+//              thread and are reduced across rows once, at the end. P^T goes
+//              to shared memory in place of the RoPE chunk, which QK no
+//              longer needs.
 //
-// Shared memory: query block (72 KB) + latent tile (128 KB) + RoPE/P^T chunk
-// (16 KB) + slot list. TMEM: S^T 64 columns, O^T 4 x 64 columns.
+// Start-up issues the dependent loads first (slot list -> block table ->
+// rows of the first tile; L2 prefetch of the later tiles' rows) and converts
+// the query block while they are in flight.
 //
-// Key splits: several CTAs may share a token; each then writes its
-// normalised partial output (fp16) with (m, l) and a merge kernel combines
-// them; a single CTA writes out/lse directly.
-// Every wait is bounded: on timeout the CTA sets NVMLA_ERRW_WAIT_TIMEOUT,
-// drains its MMAs, frees TMEM and exits.
+// Combine: a token's only CTA writes out / lse itself. With S CTAs, each
+// writes O / l (fp16) and its per-head (m, l) to the workspace (they stay in
+// L2); after one cluster barrier, CTA r weights the S partials of its share
+// of the 512 value dims by l_s 2^(m_s - M) / L (M, L over the cluster) and
+// writes bf16 out (rank 0 also writes lse). Distributed shared memory moves
+// 64 KB per CTA more slowly than this L2 round trip does on GB300.
+//
+// Shared memory: query block (72 KB, later the output staging buffer) +
+// latent tile (128 KB) + RoPE/P^T chunk (16 KB, later the combine weights) +
+// slot list. TMEM: S^T 64 columns, O^T 4 x 64 columns.
+// Every mbarrier wait is bounded: on timeout the CTA sets
+// NVMLA_ERRW_WAIT_TIMEOUT, drains its MMAs and still takes part in the
+// cluster barrier, so that every CTA of the cluster exits.
 #include "common.cuh"
 
 namespace nvmla {
@@ -70,13 +85,14 @@ __device__ unsigned long long nvmla_tc_trace[kTraceCtas][kTracePoints];
   } while (0)
 #endif
 
-constexpr int kTile = 128;          // rows per tile (MMA M)
-constexpr int kHeads = 64;          // heads per CTA (MMA N)
-constexpr int kMaxTiles = 16;       // 2048 slots
-constexpr int kThreads = 384;         // 12 warps: 3 per SM sub-partition
+constexpr int kTile = 128;           // rows per tile (MMA M)
+constexpr int kHeads = 64;           // heads per CTA (MMA N)
+constexpr int kMaxTiles = 16;        // 2048 slots
+constexpr int kThreads = 512;        // 16 warps: 4 per SM sub-partition
 constexpr int kUnpackThreads = 256;  // warps 0-7
-constexpr int kSoftmaxWarp0 = 8;     // warps 8-11; thread 256 also issues every MMA
-constexpr int kAllocWarp = 8;        // allocates and frees TMEM
+constexpr int kSoftmaxWarp0 = 8;     // warps 8-15; thread 256 also issues every MMA
+constexpr int kAllocWarp = 9;        // allocates and frees TMEM
+constexpr int kMaxCluster = 16;      // CTAs sharing one token
 constexpr int kChunkBytes = 16384;   // 128 rows x 128 bytes
 constexpr int kPieces = 12;          // 16-byte pieces of a row one unpack thread holds
 constexpr uint32_t kTmemCols = 512;
@@ -86,31 +102,30 @@ constexpr float kTau = 8.0f;         // rescale threshold, log2 units
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 
 // shared memory map (bytes); the base is 1 KB aligned
-constexpr int kOffQ = 0;                              // 9 x 8 KB: query, K-major
-constexpr int kOffL = kOffQ + 9 * 8192;               // 8 x 16 KB: latent tile
+constexpr int kOffQ = 0;                              // 9 x 8 KB: query, K-major; later output staging
+constexpr int kOffL = kOffQ + 9 * 8192;               // 8 x 16 KB: latent tile; later the fp16 partial
 constexpr int kOffR = kOffL + 8 * kChunkBytes;        // 16 KB: RoPE chunk, then P^T
 constexpr int kOffSlots = kOffR + kChunkBytes;        // kMaxTiles x 128 int32
-constexpr int kOffRed = kOffSlots + kMaxTiles * kTile * 4;  // 4 x 64 fp32
-constexpr int kOffM = kOffRed + 4 * kHeads * 4;       // 64 fp32 running maxima
-constexpr int kOffAlpha = kOffM + kHeads * 4;         // 64 fp32 rescale factors
-constexpr int kOffLsum = kOffAlpha + kHeads * 4;      // 64 fp32 final row sums
-constexpr int kOffBar = kOffLsum + kHeads * 4;
+constexpr int kOffRed = kOffSlots + kMaxTiles * kTile * 4;  // 4 quadrants x 64 heads fp32
+constexpr int kOffM = kOffRed + 4 * kHeads * 4;       // 64 fp32 running maxima (log2 units)
+constexpr int kOffAlpha = kOffM + kHeads * 4;         // 64 fp32 rescale factors, later combine weights
+constexpr int kOffMl = kOffAlpha + kHeads * 4;        // 64 x (m, l) published to the cluster
+constexpr int kOffBar = kOffMl + kHeads * 8;
 enum Bar {
-  kBarQReady = 0,    // query block converted (12 warps)
-  kBarPairFull = 1,  // 4: latent chunks 2j, 2j+1 written (8 unpack warps)
-  kBarRopeFull = 5,  // RoPE chunk written (8 unpack warps)
-  kBarLFree = 6,     // 4: PV block j done -> chunks 2j, 2j+1 reusable (commit)
-  kBarRFree = 10,    // PV done -> RoPE/P^T chunk reusable (commit)
-  kBarSFull = 11,    // QK done (commit)
-  kBarPFull = 12,    // P^T written and O^T rescaled (4 softmax warps)
-  kBarODone = 13,    // PV done (commit)
-  kBarDrain = 14,    // every MMA finished (commit)
-  kBarSlots = 15,    // slot list of tiles 1.. written (4 softmax warps)
-  kNumBars = 16
+  kBarPairFull = 0,  // 4: latent chunks 2j, 2j+1 written (8 unpack warps)
+  kBarRopeFull = 4,  // RoPE chunk written (8 unpack warps)
+  kBarLFree = 5,     // 4: PV block j done -> chunks 2j, 2j+1 reusable (commit)
+  kBarRFree = 9,     // PV done -> RoPE/P^T chunk reusable (commit)
+  kBarSFull = 10,    // QK done (commit)
+  kBarPFull = 11,    // P^T written and O^T rescaled (8 softmax warps)
+  kBarODone = 12,    // PV done (commit)
+  kBarDrain = 13,    // every MMA finished (commit)
+  kNumBars = 14
 };
 constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
 constexpr int kSmemBytes = kOffMisc + 16;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kHeads * kLatent * 2 <= 9 * 8192, "output staging fits the query region");
 
 struct Params {
   const __nv_bfloat16* q_latent;
@@ -121,9 +136,9 @@ struct Params {
   float sl2;
   __nv_bfloat16* out;
   float* lse;
-  __half* ws_o16;  // [T][S][512][H] normalised partials
-  float* ws_ml;    // [T][S][H][2] (m in log2 units, l)
-  int num_splits;
+  __half* ws_o16;   // [T][H / 64][S][8 head pieces][512][8 heads] partials O / l
+  float* ws_ml;     // [T][H / 64][S][64][2] (m in log2 units, l)
+  int num_splits;  // == cluster size
   int tiles_total;
   int32_t* err_word;
 };
@@ -279,16 +294,28 @@ __device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&r)[64
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// named barrier among the four softmax warps (id 1); the _or form returns
+// 32 consecutive TMEM columns of this thread's lane
+__device__ __forceinline__ void tmem_ld32f(uint32_t taddr, float (&r)[32]) {
+  NVMLA_TMEM_LD16F(taddr + 0, r, 0);
+  NVMLA_TMEM_LD16F(taddr + 16, r, 16);
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  NVMLA_TMEM_LD16(taddr + 0, r, 0);
+  NVMLA_TMEM_LD16(taddr + 16, r, 16);
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// named barrier among the eight softmax warps (id 1); the _or form returns
 // the OR of a predicate over the group (used to make the outcome of a
 // bounded wait, or a data-dependent branch, uniform)
-__device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 __device__ __forceinline__ bool softmax_sync_or(bool v) {
   uint32_t r;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, 1, 128, p;\n\t"
+      "bar.red.or.pred q, 1, 256, p;\n\t"
       "selp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
       : "r"(static_cast<uint32_t>(v))
@@ -314,32 +341,32 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
   return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
 }
 
-// The query block (64 heads x 576 dims, bf16 in global memory) as fp16 in
-// the K-major 128B-swizzled layout of the QK B operand. The 384 threads of
-// the unpack and softmax warps each convert 12 of the 4608 16-byte pieces;
-// all loads are issued before the first conversion so their latencies overlap.
-__device__ __forceinline__ void convert_query(const __nv_bfloat16* q_latent, const __nv_bfloat16* q_rope,
-                                              int64_t head0, uint8_t* qsmem, int tid) {
-  constexpr int kPer = kHeads * 72 / 384;  // 12
-  uint4 v[kPer];
-#pragma unroll
-  for (int n = 0; n < kPer; ++n) {
-    const int i = tid + 384 * n;
-    const int h = i / 72, j = i % 72;
-    const int64_t qh = head0 + h;
-    v[n] = j < 64 ? __ldg(reinterpret_cast<const uint4*>(q_latent + qh * kLatent) + j)
-                  : __ldg(reinterpret_cast<const uint4*>(q_rope + qh * kRope) + (j - 64));
-  }
-#pragma unroll
-  for (int n = 0; n < kPer; ++n) {
-    const int i = tid + 384 * n;
-    const int h = i / 72, j = i % 72, c = j >> 3, q = j & 7;
-    const uint32_t w[4] = {v[n].x, v[n].y, v[n].z, v[n].w};
-    uint32_t o[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) o[e] = pack_f16x2(bf16_bits_to_f32(w[e] & 0xffffu), bf16_bits_to_f32(w[e] >> 16));
-    *reinterpret_cast<uint4*>(qsmem + c * 8192 + swz(h, q)) = make_uint4(o[0], o[1], o[2], o[3]);
-  }
+// ---- cluster: rank, and a barrier over every thread of every CTA with
+// release / acquire semantics at cluster scope
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+// L2-only loads (the data was written by other CTAs of the cluster)
+__device__ __forceinline__ uint4 ldg_cg_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ float2 ldg_cg_f2(const float* p) {
+  float2 v;
+  asm volatile("ld.global.cg.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p) : "memory");
+  return v;
+}
+
+// fire-and-forget prefetch of a row into L2 (16-byte aligned, size a
+// multiple of 16)
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 // 16 E2M1 codes (8 bytes) times one scale -> two 16-byte fp16 chunks
@@ -356,14 +383,14 @@ __device__ __forceinline__ void zero_row(uint8_t* dst_base, int r) {
   for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(dst_base + swz(r, c)) = make_uint4(0, 0, 0, 0);
 }
 
-// transposing butterfly: 64 values per lane -> lane L holds the reduction
-// over the warp's 32 lanes for heads 2L and 2L+1 (in v[0], v[1])
+// transposing butterfly: 32 values per lane -> lane L holds the reduction
+// over the warp's 32 lanes of value L (in v[0])
 template <bool kMax>
-__device__ __forceinline__ void warp_reduce64(float (&v)[64], int lane) {
+__device__ __forceinline__ void warp_reduce32(float (&v)[32], int lane) {
 #pragma unroll
   for (int step = 0; step < 5; ++step) {
     const int o = 16 >> step;
-    const int n = 32 >> step;  // values kept after this step
+    const int n = 16 >> step;  // values kept after this step
     const bool upper = (lane & o) != 0;
 #pragma unroll
     for (int i = 0; i < n; ++i) {
@@ -380,13 +407,6 @@ __device__ __forceinline__ void warp_reduce64(float (&v)[64], int lane) {
 // pieces (16, 17) and its half of the RoPE bytes (18 + 2h, 19 + 2h).
 __device__ __forceinline__ int piece_of(int n, int h) {
   return n < 8 ? 2 * (2 * (n >> 1) + h) + (n & 1) : (n < 10 ? 16 + (n - 8) : 18 + 2 * h + (n - 10));
-}
-
-__device__ __forceinline__ void load_row(const uint8_t* cache, int32_t slot, int h, uint4 (&raw)[kPieces]) {
-  if (slot < 0) return;
-  const uint4* row = reinterpret_cast<const uint4*>(cache + static_cast<int64_t>(slot) * kRowBytes);
-#pragma unroll
-  for (int n = 0; n < kPieces; ++n) raw[n] = __ldg(row + piece_of(n, h));
 }
 
 // latent chunk c = 2j + h of one row (64 dims) from the held pieces
@@ -436,32 +456,37 @@ __device__ __forceinline__ int32_t ldg_nc_s32(const int32_t* p) {
   return v;
 }
 
-// row pieces of one unpack thread; the loads are volatile so that they are
-// issued here (one tile ahead) and not sunk next to their first use
-__device__ __forceinline__ void load_row_now(const uint8_t* cache, int32_t slot, int h, uint4 (&raw)[kPieces]) {
+// Held pieces n0 .. n1-1 of the row in slot `slot` (nothing for a masked
+// slot). The loads are volatile so that they are issued here, as soon as the
+// registers are free, and not sunk next to their first use.
+__device__ __forceinline__ void load_pieces(const uint8_t* cache, int32_t slot, int h, uint4 (&raw)[kPieces], int n0,
+                                            int n1) {
   if (slot < 0) return;
   const uint8_t* row = cache + static_cast<int64_t>(slot) * kRowBytes;
 #pragma unroll
-  for (int n = 0; n < kPieces; ++n) raw[n] = ldg_nc_v4(row + 16 * piece_of(n, h));
+  for (int n = 0; n < kPieces; ++n)
+    if (n >= n0 && n < n1) raw[n] = ldg_nc_v4(row + 16 * piece_of(n, h));
 }
 
 __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int split = blockIdx.x, t = blockIdx.y, h0 = blockIdx.z * kHeads;
+  const int t = blockIdx.y, h0 = blockIdx.z * kHeads;
+  const int S = p.num_splits;
+  const uint32_t rank = cluster_rank();  // the CTA's split: clusters span blockIdx.x
 
   int32_t* slots = reinterpret_cast<int32_t*>(smem + kOffSlots);
   float* red = reinterpret_cast<float*>(smem + kOffRed);
   float* m_run = reinterpret_cast<float*>(smem + kOffM);
   float* alpha_s = reinterpret_cast<float*>(smem + kOffAlpha);
-  float* lsum = reinterpret_cast<float*>(smem + kOffLsum);
+  float* ml_pub = reinterpret_cast<float*>(smem + kOffMl);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
   auto bar = [&](int i) { return sbase + kOffBar + 8 * i; };
 
-  const int tile_lo = (split * p.tiles_total) / p.num_splits;
-  const int tile_hi = ((split + 1) * p.tiles_total) / p.num_splits;
+  const int tile_lo = (static_cast<int>(rank) * p.tiles_total) / S;
+  const int tile_hi = ((static_cast<int>(rank) + 1) * p.tiles_total) / S;
   const int kbeg = tile_lo * kTile;
   const int kend = min(tile_hi * kTile, p.topk);
   const int nkeys = max(0, kend - kbeg);
@@ -473,14 +498,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
   const int32_t seq = p.sel.q_seq_idx ? __ldg(p.sel.q_seq_idx + t) : 0;
   const int32_t* bt_row = p.sel.block_table + static_cast<int64_t>(seq) * p.sel.max_pages;
   const int32_t* idx_row = p.sel.topk_idx + static_cast<int64_t>(t) * p.topk;
-  auto limit_of = [&]() -> int64_t {
-    int64_t lim = static_cast<int64_t>(p.sel.max_pages) * kPage;
-    if (p.sel.seq_lens) {
-      const int64_t L = __ldg(p.sel.seq_lens + seq);
-      lim = L < lim ? L : lim;
-    }
-    return lim;
-  };
   // slot of position pos (-1 for padding or a bad entry, which is reported
   // when `report`)
   auto slot_of_pos = [&](int32_t pos, int64_t limit, bool report) -> int32_t {
@@ -498,13 +515,28 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
     return static_cast<int32_t>(s);
   };
 
-  // ---- loads that do not depend on shared memory start before setup
+  // ---- start-up: the dependent loads first (slot list, block table, rows),
+  // the query block while they are in flight
+  const bool is_unpack = tid < kUnpackThreads;
   const int ur = tid & 127, uh = (tid >> 7) & 1;  // unpack threads: row, part
-  uint4 rawA[kPieces], rawB[kPieces];
-  int32_t slotA = -1, slotB = -1;
+  const int sj = tid - kUnpackThreads;            // softmax threads: 0..255
+  uint4 raw[kPieces];
+  int32_t slot0 = -1;
   int32_t pos0 = -1;
-  if (tid < kUnpackThreads && kbeg + ur < kend) pos0 = ldg_nc_s32(idx_row + kbeg + ur);
-  constexpr int kQPer = kHeads * 72 / kThreads;  // 12 query pieces per thread
+  constexpr int kLaterPer = kMaxTiles / 2;  // later tiles per softmax thread
+  int32_t posl[kLaterPer];
+  if (is_unpack) {
+    if (kbeg + ur < kend) pos0 = ldg_nc_s32(idx_row + kbeg + ur);
+  } else {
+    // softmax thread sj handles row sj % 128 of tiles 1 + sj / 128 + 2m
+#pragma unroll
+    for (int m = 0; m < kLaterPer; ++m) {
+      const int i = 1 + (sj >> 7) + 2 * m;
+      const int key = kbeg + i * kTile + (sj & 127);
+      posl[m] = (i < ntiles && key < kend) ? ldg_nc_s32(idx_row + key) : -1;
+    }
+  }
+  constexpr int kQPer = kHeads * 72 / kThreads;  // 9 query pieces per thread
   uint4 qv[kQPer];
 #pragma unroll
   for (int n = 0; n < kQPer; ++n) {
@@ -513,10 +545,31 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
     const int64_t qh = static_cast<int64_t>(t) * p.H + h0 + h;
     qv[n] = j < 64 ? ldg_nc_v4(p.q_latent + qh * kLatent + 8 * j) : ldg_nc_v4(p.q_rope + qh * kRope + 8 * (j - 64));
   }
+  int64_t limit = static_cast<int64_t>(p.sel.max_pages) * kPage;
+  if (p.sel.seq_lens) {
+    const int64_t L = __ldg(p.sel.seq_lens + seq);
+    limit = L < limit ? L : limit;
+  }
+  const bool report = blockIdx.z == 0;  // one head block reports bad entries
+  if (is_unpack) {
+    if (ntiles > 0 && kbeg + ur < kend) slot0 = slot_of_pos(pos0, limit, report && uh == 0);
+    load_pieces(p.cache, slot0, uh, raw, 0, kPieces);
+    if (uh == 0) slots[ur] = slot0;
+  } else {
+#pragma unroll
+    for (int m = 0; m < kLaterPer; ++m) {
+      const int i = 1 + (sj >> 7) + 2 * m;
+      if (i < ntiles) {
+        const int32_t s = slot_of_pos(posl[m], limit, report);
+        slots[i * kTile + (sj & 127)] = s;
+        if (s >= 0) prefetch_l2(p.cache + static_cast<int64_t>(s) * kRowBytes, kRowBytes);
+      }
+    }
+  }
+  if (tid == 0) NVMLA_TRACE_POINT(41);
 
   // ---- setup
   if (tid == kThreads - 1) {
-    mbar_init(bar(kBarQReady), 12);
     for (int j = 0; j < 4; ++j) {
       mbar_init(bar(kBarPairFull + j), 8);
       mbar_init(bar(kBarLFree + j), 1);
@@ -524,9 +577,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
     mbar_init(bar(kBarRopeFull), 8);
     mbar_init(bar(kBarRFree), 1);
     mbar_init(bar(kBarSFull), 1);
-    mbar_init(bar(kBarPFull), 4);
+    mbar_init(bar(kBarPFull), 8);
     mbar_init(bar(kBarODone), 1);
-    mbar_init(bar(kBarSlots), 4);
     mbar_init(bar(kBarDrain), 1);
     *abort_flag = (sbase & 1023u) ? 1 : 0;  // swizzled operands need a 1 KB aligned base
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -538,14 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  if (*abort_flag && tid == 0) report_error(p.err_word, NVMLA_ERRW_WAIT_TIMEOUT, 1);
-  if (tid == 0) NVMLA_TRACE_POINT(0);
-
-  // query block -> fp16, K-major 128B-swizzled (all 12 warps)
+  // query block -> fp16, K-major 128B-swizzled (all 16 warps)
 #pragma unroll
   for (int n = 0; n < kQPer; ++n) {
     const int i = tid + kThreads * n;
@@ -557,87 +602,68 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
     *reinterpret_cast<uint4*>(smem + kOffQ + c * 8192 + swz(h, q)) = make_uint4(o[0], o[1], o[2], o[3]);
   }
   fence_async_smem();
-  warp_arrive(bar(kBarQReady), lane);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  if (*abort_flag && tid == 0) report_error(p.err_word, NVMLA_ERRW_WAIT_TIMEOUT, 1);
+  if (tid == 0) NVMLA_TRACE_POINT(0);
 
-  if (tid < kUnpackThreads) {
+  // roles; the softmax group's epilogue ends with the (m, l) of every head
+  // published in ml_pub
+  const int sw = warp - kSoftmaxWarp0;       // softmax warp 0..7
+  const int quad = sw & 3, hh = sw >> 2;     // TMEM lane quadrant, head half
+  const int hb = hh * 32;                    // first head of this thread
+  const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+  bool ok = true;
+  if (is_unpack) {
     // ------------------------------------------------------------ unpack
-    // tile 0: page of the row, then its pieces (errors reported by part 0;
-    // the softmax warps build the slot list of the later tiles)
-    if (ntiles > 0) {
-      slotA = (kbeg + ur < kend) ? slot_of_pos(pos0, limit_of(), uh == 0 && blockIdx.z == 0) : -1;
-      if (tid == 0) NVMLA_TRACE_POINT(41);
-      load_row_now(p.cache, slotA, uh, rawA);
-      if (uh == 0) slots[ur] = slotA;
-    }
-    if (tid == 0) NVMLA_TRACE_POINT(13);
-    bool ok = *abort_flag == 0;
-    auto wait_warp = [&](uint32_t b, uint32_t parity) -> bool {
-      return wait_bar_warp(b, parity, abort_flag, p.err_word);
-    };
-    // one tile: chunks are written as the previous tile's PV frees them; the
-    // next tile's rows are requested after the first pair
-    auto tile = [&](int i, const uint4 (&cur)[kPieces], int32_t cur_slot, uint4 (&nxt)[kPieces],
-                    int32_t& nxt_slot) -> bool {
+    ok = *abort_flag == 0;
+    int32_t cur_slot = slot0;
+    for (int i = 0; i < ntiles && ok; ++i) {
       const bool valid = cur_slot >= 0;
+      const int32_t nxt_slot = (i + 1 < ntiles) ? slots[(i + 1) * kTile + ur] : -1;
       if (tid == 0 && i < 2) {
-        uint32_t x = cur[0].x ^ cur[11].w;  // first use: the pieces have arrived
+        uint32_t x = raw[0].x ^ raw[11].w;  // first use: the pieces have arrived
         asm volatile("" ::"r"(x));
         NVMLA_TRACE_POINT(44 + i);
       }
-      for (int j = 0; j < 4; ++j) {
-        if (i >= 1 && !wait_warp(bar(kBarLFree + j), (i - 1) & 1)) return false;
+      for (int j = 0; j < 4 && ok; ++j) {
+        if (i >= 1) ok = wait_bar_warp(bar(kBarLFree + j), (i - 1) & 1, abort_flag, p.err_word);
+        if (!ok) break;
         uint8_t* chunk = smem + kOffL + (2 * j + uh) * kChunkBytes;
         if (valid) {
-          write_latent(cur, j, uh, chunk, ur);
+          write_latent(raw, j, uh, chunk, ur);
         } else {
           zero_row(chunk, ur);
         }
         fence_async_smem();
         warp_arrive(bar(kBarPairFull + j), lane);
-        if (j == 0 && i + 1 < ntiles) {
-          if (i == 0 && !wait_warp(bar(kBarSlots), 0)) return false;
-          nxt_slot = slots[(i + 1) * kTile + ur];
-          load_row_now(p.cache, nxt_slot, uh, nxt);
-        }
+        // the registers of this pair (and of a scale piece once its last
+        // pair is written) now take the next tile's row
+        load_pieces(p.cache, nxt_slot, uh, raw, 2 * j, 2 * j + 2);
+        if (j == 1) load_pieces(p.cache, nxt_slot, uh, raw, 8, 9);
+        if (j == 3) load_pieces(p.cache, nxt_slot, uh, raw, 9, 10);
       }
-      if (i >= 1 && !wait_warp(bar(kBarRFree), (i - 1) & 1)) return false;
+      if (ok && i >= 1) ok = wait_bar_warp(bar(kBarRFree), (i - 1) & 1, abort_flag, p.err_word);
+      if (!ok) break;
       uint8_t* rc = smem + kOffR;
       if (valid) {
-        write_rope(cur, uh, rc, ur);
+        write_rope(raw, uh, rc, ur);
       } else {
 #pragma unroll
         for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(rc + swz(ur, 4 * uh + c)) = make_uint4(0, 0, 0, 0);
       }
       fence_async_smem();
       warp_arrive(bar(kBarRopeFull), lane);
-      return true;
-    };
-    // tiles alternate between the two register sets
-    for (int i = 0; i < ntiles && ok; i += 2) {
-      ok = tile(i, rawA, slotA, rawB, slotB);
+      load_pieces(p.cache, nxt_slot, uh, raw, 10, 12);
+      cur_slot = nxt_slot;
       if (tid == 0 && i < 4) NVMLA_TRACE_POINT(14 + i);
-      if (ok && i + 1 < ntiles) ok = tile(i + 1, rawB, slotB, rawA, slotA);
-      if (tid == 0 && i + 1 < 4) NVMLA_TRACE_POINT(15 + i);
     }
   } else {
     // ------------------------------------------------------------ softmax
-    const int sw = warp - kSoftmaxWarp0;  // 0..3 = TMEM lane quadrant
-    const int k = sw * 32 + lane;          // row of this thread
+    const int k = quad * 32 + lane;  // row of this thread
     const bool issuer = tid == kUnpackThreads;
-    // slot list of this thread's row in the later tiles
-    {
-      const int64_t limit = limit_of();
-      int32_t pos[kMaxTiles];
-#pragma unroll
-      for (int i = 1; i < kMaxTiles; ++i) {
-        const int key = kbeg + i * kTile + k;
-        pos[i] = (i < ntiles && key < kend) ? ldg_nc_s32(idx_row + key) : -1;
-      }
-#pragma unroll
-      for (int i = 1; i < kMaxTiles; ++i)
-        if (i < ntiles) slots[i * kTile + k] = slot_of_pos(pos[i], limit, blockIdx.z == 0);
-      warp_arrive(bar(kBarSlots), lane);
-    }
     constexpr uint32_t idesc_qk = idesc_f16(false, false);
     constexpr uint32_t idesc_pv = idesc_f16(true, true);
     const uint32_t lb = sbase + kOffL, rb = sbase + kOffR, qb = sbase + kOffQ;
@@ -645,7 +671,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
     // then the RoPE chunk
     auto issue_qk = [&](int i) -> bool {
       const uint32_t par = i & 1;
-      if (i == 0 && !wait_bar(bar(kBarQReady), 0, abort_flag, p.err_word)) return false;
       for (int j = 0; j < 4; ++j) {
         if (!wait_bar(bar(kBarPairFull + j), par, abort_flag, p.err_word)) return false;
         tc_fence_after();
@@ -685,17 +710,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
       return true;
     };
 
-    const uint32_t lane_base = static_cast<uint32_t>(sw * 32) << 16;
-    float lp[64];  // this row's share of every head's sum
+    float lp[32];  // this row's share of its heads' sums
 #pragma unroll
-    for (int h = 0; h < 64; ++h) lp[h] = 0.f;
-    bool ok = !softmax_sync_or(*abort_flag != 0);
+    for (int h = 0; h < 32; ++h) lp[h] = 0.f;
+    ok = !softmax_sync_or(*abort_flag != 0);
     // the issuer's outcome is made uniform across its warp before any
     // warp-collective operation
     auto issued = [&](bool mine) -> bool { return __shfl_sync(0xffffffffu, mine, 0); };
     for (int i = 0; i < ntiles && ok; ++i) {
+      // a failed PV issue of the previous tile left the abort flag raised;
+      // the issuer then issues nothing more, and the OR below ends the loop
+      // for the whole group at once
       bool okq = true;
-      if (issuer) okq = issue_qk(i);
+      if (issuer) okq = *abort_flag == 0 && issue_qk(i);
       ok = issued(okq);
       if (ok) ok = wait_bar_warp(bar(kBarSFull), i & 1, abort_flag, p.err_word);
       if (softmax_sync_or(!ok)) {
@@ -705,29 +732,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
       tc_fence_after();
       if (tid == 256 && i < 4) NVMLA_TRACE_POINT(21 + 3 * i);
       const bool valid = slots[i * kTile + k] >= 0;
-      float s[64];
-      tmem_ld64f(tmem + lane_base + kColS, s);
-      if (tid == 256 && i < 2) NVMLA_TRACE_POINT(50 + 8 * i);
+      float s[32];
+      tmem_ld32f(tmem + lane_base + kColS + hb, s);
 #pragma unroll
-      for (int h = 0; h < 64; ++h) s[h] = valid ? s[h] * p.sl2 : -INFINITY;
+      for (int h = 0; h < 32; ++h) s[h] = valid ? s[h] * p.sl2 : -INFINITY;
       // does any score exceed its head's running maximum by more than 2^tau?
       float excess = -INFINITY;
       if (valid) {
 #pragma unroll
-        for (int h = 0; h < 64; ++h) excess = fmaxf(excess, s[h] - m_run[h]);
+        for (int h = 0; h < 32; ++h) excess = fmaxf(excess, s[h] - m_run[hb + h]);
       }
       const bool slow = softmax_sync_or(excess > kTau);
-      if (tid == 256 && i < 2) NVMLA_TRACE_POINT(51 + 8 * i);
       if (slow) {
         // exact per-head maximum of this tile (destroys s; reloaded below)
-        warp_reduce64<true>(s, lane);
-        if (tid == 256 && i < 2) NVMLA_TRACE_POINT(52 + 8 * i);
-        red[sw * 64 + 2 * lane] = s[0];
-        red[sw * 64 + 2 * lane + 1] = s[1];
+        warp_reduce32<true>(s, lane);
+        red[quad * 64 + hb + lane] = s[0];
         softmax_sync();
-        if (tid == 256 && i < 2) NVMLA_TRACE_POINT(53 + 8 * i);
-        if (sw < 2) {
-          const int h = k;
+        if (quad == 0) {
+          const int h = hb + lane;
           const float mt = fmaxf(fmaxf(red[h], red[64 + h]), fmaxf(red[128 + h], red[192 + h]));
           const float mo = m_run[h];
           const float mn = fmaxf(mo, mt);
@@ -735,189 +757,238 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
           m_run[h] = mn;
         }
         softmax_sync();
-        if (tid == 256 && i < 2) NVMLA_TRACE_POINT(54 + 8 * i);
 #pragma unroll
-        for (int h = 0; h < 64; ++h) lp[h] *= alpha_s[h];
+        for (int h = 0; h < 32; ++h) lp[h] *= alpha_s[hb + h];
         if (i >= 1) {
           // O^T holds the finished PV of the earlier tiles (QK of this tile
           // could only start after the last of them); 16 columns at a time
 #pragma unroll 1
-          for (int jq = 0; jq < 16; ++jq) {
-            const uint32_t ta = tmem + lane_base + kColO + 16 * jq;
+          for (int jq = 0; jq < 8; ++jq) {
+            const uint32_t col = kColO + 64 * (jq >> 1) + hb + 16 * (jq & 1);
             uint32_t orr[16];
-            NVMLA_TMEM_LD16(ta, orr, 0);
+            NVMLA_TMEM_LD16(tmem + lane_base + col, orr, 0);
             asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-            const float* al = alpha_s + 16 * (jq & 3);
+            const float* al = alpha_s + hb + 16 * (jq & 1);
 #pragma unroll
             for (int e = 0; e < 16; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * al[e]);
-            NVMLA_TMEM_ST16(ta, orr, 0);
+            NVMLA_TMEM_ST16(tmem + lane_base + col, orr, 0);
           }
           asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         }
-        if (tid == 256 && i < 2) NVMLA_TRACE_POINT(55 + 8 * i);
-        tmem_ld64f(tmem + lane_base + kColS, s);
+        tmem_ld32f(tmem + lane_base + kColS + hb, s);
 #pragma unroll
-        for (int h = 0; h < 64; ++h) s[h] = valid ? s[h] * p.sl2 : -INFINITY;
-        if (tid == 256 && i < 2) NVMLA_TRACE_POINT(56 + 8 * i);
+        for (int h = 0; h < 32; ++h) s[h] = valid ? s[h] * p.sl2 : -INFINITY;
       }
       if (tid == 256 && i < 4) NVMLA_TRACE_POINT(22 + 3 * i);
       // P = 2^(s - m); masked rows give 0
 #pragma unroll
-      for (int h = 0; h < 64; ++h) {
-        const float pv = valid ? ex2(s[h] - m_run[h]) : 0.f;
+      for (int h = 0; h < 32; ++h) {
+        const float pv = valid ? ex2(s[h] - m_run[hb + h]) : 0.f;
         s[h] = pv;
         lp[h] += pv;
       }
-      // P^T row -> the RoPE chunk's place (QK of this tile is complete)
+      // P^T row (this thread's 32 heads) -> the RoPE chunk's place (QK of
+      // this tile is complete)
       uint8_t* pt = smem + kOffR;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
+      for (int cc = 0; cc < 4; ++cc) {
         uint4 q;
-        q.x = pack_f16x2(s[8 * c + 0], s[8 * c + 1]);
-        q.y = pack_f16x2(s[8 * c + 2], s[8 * c + 3]);
-        q.z = pack_f16x2(s[8 * c + 4], s[8 * c + 5]);
-        q.w = pack_f16x2(s[8 * c + 6], s[8 * c + 7]);
-        *reinterpret_cast<uint4*>(pt + swz(k, c)) = q;
+        q.x = pack_f16x2(s[8 * cc + 0], s[8 * cc + 1]);
+        q.y = pack_f16x2(s[8 * cc + 2], s[8 * cc + 3]);
+        q.z = pack_f16x2(s[8 * cc + 4], s[8 * cc + 5]);
+        q.w = pack_f16x2(s[8 * cc + 6], s[8 * cc + 7]);
+        *reinterpret_cast<uint4*>(pt + swz(k, 4 * hh + cc)) = q;
       }
       fence_async_smem();
       tc_fence_before();
       warp_arrive(bar(kBarPFull), lane);
       if (tid == 256 && i < 4) NVMLA_TRACE_POINT(23 + 3 * i);
-      bool okp = true;
-      if (issuer) okp = issue_pv(i);
-      ok = issued(okp);
+      if (issuer) issue_pv(i);
     }
-    // ------------------------------------------------------------ epilogue
+    // ------------------------------------------------------------ row sums
     if (ok && ntiles > 0) ok = wait_bar_warp(bar(kBarODone), (ntiles - 1) & 1, abort_flag, p.err_word);
     ok = !softmax_sync_or(!ok);
+    tc_fence_after();
     if (tid == 256) NVMLA_TRACE_POINT(33);
-    if (ok) {
-      // row sums of every head, reduced across the 128 rows
-      warp_reduce64<false>(lp, lane);
-      red[sw * 64 + 2 * lane] = lp[0];
-      red[sw * 64 + 2 * lane + 1] = lp[1];
-      softmax_sync();
-      if (sw < 2) {
-        const float l = (red[k] + red[64 + k]) + (red[128 + k] + red[192 + k]);
-        lsum[k] = l;
-        alpha_s[k] = l > 0.f ? 1.f / l : 0.f;  // reused: 1 / l of every head
-      }
-      softmax_sync();
-      tc_fence_after();
-      const int64_t tok = t;
-      for (int j = 0; j < 4; ++j) {
-        uint32_t orr[64];
-        if (ntiles > 0) {
-          tmem_ld64(tmem + lane_base + kColO + 64 * j, orr);
-        } else {
-#pragma unroll
-          for (int h = 0; h < 64; ++h) orr[h] = 0u;
-        }
-        const int dv = 128 * j + k;
-        if (p.num_splits == 1) {
-#pragma unroll
-          for (int h = 0; h < 64; ++h)
-            p.out[(tok * p.H + h0 + h) * kLatent + dv] = __float2bfloat16_rn(__uint_as_float(orr[h]) * alpha_s[h]);
-        } else {
-          // normalised partial o = O / l as fp16, 64 heads of one value dim
-          // contiguous: eight 16-byte stores
-          __half* dst = p.ws_o16 + ((tok * p.num_splits + split) * kLatent + dv) * p.H + h0;
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            uint32_t w4[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int h = 8 * c + 2 * e;
-              w4[e] = pack_f16x2(__uint_as_float(orr[h]) * alpha_s[h], __uint_as_float(orr[h + 1]) * alpha_s[h + 1]);
-            }
-            reinterpret_cast<uint4*>(dst)[c] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-          }
-        }
-      }
-      if (sw < 2) {
-        const int h = k;
-        const float m = m_run[h], l = lsum[h];
-        if (p.num_splits == 1) {
-          p.lse[tok * p.H + h0 + h] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
-        } else {
-          const int64_t base = (tok * p.num_splits + split) * p.H + h0;
-          p.ws_ml[(base + h) * 2] = l > 0.f ? m : -INFINITY;
-          p.ws_ml[(base + h) * 2 + 1] = l;
-        }
-      }
+    warp_reduce32<false>(lp, lane);
+    red[quad * 64 + hb + lane] = lp[0];
+    softmax_sync();
+    if (quad == 0) {
+      const int h = hb + lane;
+      const float l = (red[h] + red[64 + h]) + (red[128 + h] + red[192 + h]);
+      const bool live = ok && l > 0.f;
+      ml_pub[2 * h] = live ? m_run[h] : -INFINITY;
+      ml_pub[2 * h + 1] = live ? l : 0.f;
+      alpha_s[h] = live ? 1.f / l : 0.f;
     }
-    if (tid == 256) NVMLA_TRACE_POINT(35);
     if (issuer) {
       // every MMA issued has finished once this commit lands
       mma_commit(bar(kBarDrain));
       wait_bar_drain(bar(kBarDrain), 0);
     }
-    tc_fence_before();
   }
 
-  __syncthreads();
+  // ------------------------------------------------------------ combine
+  if (S == 1) {
+    // the token's only CTA: O / l as bf16 [64 heads][512 dims] staged in the
+    // query block's place, then 16-byte stores of out
+    __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(smem + kOffQ);
+    __syncthreads();  // alpha_s (1 / l) of every head is written
+    if (!is_unpack) {
+#pragma unroll 1
+      for (int j = 0; j < 4; ++j) {
+        const int dv = 128 * j + quad * 32 + lane;
+        uint32_t o[32];
+        if (ok && ntiles > 0) {
+          tmem_ld32(tmem + lane_base + kColO + 64 * j + hb, o);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = 0u;
+        }
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          stage[(hb + e) * kLatent + dv] = __float2bfloat16_rn(__uint_as_float(o[e]) * alpha_s[hb + e]);
+      }
+      tc_fence_before();
+      if (quad == 0) {
+        const int h = hb + lane;
+        const float m = ml_pub[2 * h], l = ml_pub[2 * h + 1];
+        p.lse[static_cast<int64_t>(t) * p.H + h0 + h] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+      }
+    }
+    __syncthreads();
+    if (warp == kAllocWarp) {
+      tc_fence_after();
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    }
+#pragma unroll
+    for (int u = 0; u < kHeads * (kLatent / 8) / kThreads; ++u) {
+      const int pc = tid + kThreads * u, h = pc >> 6, g = pc & 63;
+      const uint4 v = *reinterpret_cast<const uint4*>(stage + h * kLatent + 8 * g);
+      *reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(t) * p.H + h0 + h) * kLatent + 8 * g) = v;
+    }
+  } else {
+    // S CTAs: each writes O / l (fp16, 8-head pieces x 512 dims) and its (m, l) to
+    // the workspace; after a cluster barrier CTA `rank` combines the S
+    // partials of its share [dv0, dv0 + ndv) of the value dims
+    const int64_t cbase = (static_cast<int64_t>(t) * gridDim.z + blockIdx.z) * S;  // first split of this cluster
+    __syncthreads();  // alpha_s (1 / l) of every head is written
+    if (!is_unpack) {
+      __half* wo = p.ws_o16 + (cbase + rank) * (kLatent * kHeads);
+#pragma unroll 1
+      for (int j = 0; j < 4; ++j) {
+        const int dv = 128 * j + quad * 32 + lane;
+        uint32_t o[32];
+        if (ok && ntiles > 0) {
+          tmem_ld32(tmem + lane_base + kColO + 64 * j + hb, o);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = 0u;
+        }
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t w4[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int hl = 8 * cc + 2 * e;
+            w4[e] = pack_f16x2(__uint_as_float(o[hl]) * alpha_s[hb + hl],
+                               __uint_as_float(o[hl + 1]) * alpha_s[hb + hl + 1]);
+          }
+          // piece-major [8 head pieces][512 dims][8 heads]: a warp's lanes
+          // (consecutive dims) store 512 contiguous bytes
+          *reinterpret_cast<uint4*>(wo + ((4 * hh + cc) * kLatent + dv) * 8) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        }
+      }
+      tc_fence_before();
+      if (quad == 0) {
+        const int h = hb + lane;
+        *reinterpret_cast<float2*>(p.ws_ml + ((cbase + rank) * kHeads + h) * 2) =
+            make_float2(ml_pub[2 * h], ml_pub[2 * h + 1]);
+      }
+    }
+    // release / acquire at cluster scope: every partial of the cluster is
+    // visible to every CTA of it
+    cluster_sync_all();
+    if (tid == 256) NVMLA_TRACE_POINT(35);
+    if (warp == kAllocWarp) {
+      tc_fence_after();
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    }
+    const int dv0 = 8 * ((static_cast<int>(rank) * (kLatent / 8)) / S);
+    const int ndv = 8 * (((static_cast<int>(rank) + 1) * (kLatent / 8)) / S) - dv0;
+    const int nitems = ndv * 8;  // (dim, 8-head piece)
+    const __half* wo0 = p.ws_o16 + cbase * (kLatent * kHeads);
+    uint4 v[8];
+    auto load_batch = [&](int item, int s0) {
+      const int piece = item / ndv, dl = item - piece * ndv;
+      const int64_t off = static_cast<int64_t>(piece * kLatent + dv0 + dl) * 8;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (s0 + u < S) v[u] = ldg_cg_v4(wo0 + static_cast<int64_t>(s0 + u) * (kLatent * kHeads) + off);
+    };
+    // this thread's first partials are requested before the weights are known
+    if (tid < nitems) load_batch(tid, 0);
+    float* coef = reinterpret_cast<float*>(smem + kOffR);  // [S][64] combine weights
+    if (tid < kHeads) {
+      const int h = tid;
+      float2 ml[kMaxCluster];
+#pragma unroll
+      for (int s = 0; s < kMaxCluster; ++s)
+        if (s < S) ml[s] = ldg_cg_f2(p.ws_ml + ((cbase + s) * kHeads + h) * 2);
+      float M = -INFINITY;
+#pragma unroll
+      for (int s = 0; s < kMaxCluster; ++s)
+        if (s < S) M = fmaxf(M, ml[s].x);
+      float L = 0.f;
+#pragma unroll
+      for (int s = 0; s < kMaxCluster; ++s) {
+        if (s < S) {
+          const float w = ml[s].y > 0.f ? ml[s].y * ex2(ml[s].x - M) : 0.f;
+          ml[s].y = w;
+          L += w;
+        }
+      }
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+      for (int s = 0; s < kMaxCluster; ++s)
+        if (s < S) coef[s * kHeads + h] = ml[s].y * inv;
+      if (rank == 0) p.lse[static_cast<int64_t>(t) * p.H + h0 + h] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+    }
+    __syncthreads();
+    if (tid == 256) NVMLA_TRACE_POINT(36);
+    __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(smem + kOffQ);  // [64 heads][ndv]
+    for (int it = tid; it < nitems; it += kThreads) {
+      const int piece = it / ndv, dl = it - piece * ndv;
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      for (int s0 = 0; s0 < S; s0 += 8) {
+        if (s0 > 0 || it != tid) load_batch(it, s0);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          if (s0 + u < S) {
+            const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+            const float* c = coef + (s0 + u) * kHeads + 8 * piece;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+              acc[2 * e] += c[2 * e] * f.x;
+              acc[2 * e + 1] += c[2 * e + 1] * f.y;
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) stage[(8 * piece + e) * ndv + dl] = __float2bfloat16_rn(acc[e]);
+    }
+    __syncthreads();
+    if (tid == 256) NVMLA_TRACE_POINT(38);
+    const int per_head = ndv / 8;
+    for (int pc = tid; pc < kHeads * per_head; pc += kThreads) {
+      const int h = pc / per_head, g = pc - h * per_head;
+      const uint4 w = *reinterpret_cast<const uint4*>(stage + h * ndv + 8 * g);
+      *reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(t) * p.H + h0 + h) * kLatent + dv0 + 8 * g) = w;
+    }
+  }
   if (tid == 0) NVMLA_TRACE_POINT(34);
-  if (warp == kAllocWarp) {
-    tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
-  }
-}
-
-// Merge of the fp16 partials of S key splits for one (token, 64-head block,
-// 32 value dims): with M = max_s m_s, L = sum_s l_s 2^(m_s - M) and
-// w_s = l_s 2^(m_s - M) / L, out[h][d] = sum_s w_s o_s[d][h] (bf16) and
-// lse = (M + log2 L) ln 2 (written by the first dim block).
-constexpr int kMergeDims = 32;
-__global__ void __launch_bounds__(256) merge_tc_kernel(const __half* __restrict__ ws_o16,
-                                                       const float* __restrict__ ws_ml, int S, int H,
-                                                       __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
-  __shared__ float wgt[kMaxTiles][kHeads];
-  __shared__ float tileo[kMergeDims][kHeads + 1];
-  const int t = blockIdx.x, h0 = blockIdx.y * kHeads, d0 = blockIdx.z * kMergeDims, tid = threadIdx.x;
-  if (tid < kHeads) {
-    const int h = h0 + tid;
-    float M = -INFINITY;
-    for (int s = 0; s < S; ++s) M = fmaxf(M, ws_ml[((static_cast<int64_t>(t) * S + s) * H + h) * 2]);
-    float L = 0.f;
-    for (int s = 0; s < S; ++s) {
-      const float2 ml = *reinterpret_cast<const float2*>(ws_ml + ((static_cast<int64_t>(t) * S + s) * H + h) * 2);
-      const float w = (ml.x == -INFINITY) ? 0.f : ml.y * exp2f(ml.x - M);
-      wgt[s][tid] = w;
-      L += w;
-    }
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    for (int s = 0; s < S; ++s) wgt[s][tid] *= inv;
-    if (blockIdx.z == 0) lse[static_cast<int64_t>(t) * H + h] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
-  }
-  __syncthreads();
-  // thread (d = tid / 8, heads 8 (tid % 8) .. +7)
-  const int dl = tid >> 3, hq = (tid & 7) * 8;
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  for (int s = 0; s < S; ++s) {
-    const uint4 v = *reinterpret_cast<const uint4*>(ws_o16 + ((static_cast<int64_t>(t) * S + s) * kLatent + d0 + dl) * H +
-                                                    h0 + hq);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const __half2 h2 = *reinterpret_cast<const __half2*>(&w[e]);
-      const float2 f = __half22float2(h2);
-      acc[2 * e] += wgt[s][hq + 2 * e] * f.x;
-      acc[2 * e + 1] += wgt[s][hq + 2 * e + 1] * f.y;
-    }
-  }
-#pragma unroll
-  for (int e = 0; e < 8; ++e) tileo[dl][hq + e] = acc[e];
-  __syncthreads();
-  // transposed write: thread (head h = tid / 4, dims 8 (tid % 4) .. +7)
-  const int h = tid >> 2, dq = (tid & 3) * 8;
-  uint32_t o[4];
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const __nv_bfloat162 b = __floats2bfloat162_rn(tileo[dq + 2 * e][h], tileo[dq + 2 * e + 1][h]);
-    o[e] = *reinterpret_cast<const uint32_t*>(&b);
-  }
-  *reinterpret_cast<uint4*>(out + (static_cast<int64_t>(t) * H + h0 + h) * kLatent + d0 + dq) =
-      make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 }  // namespace tc
@@ -925,19 +996,82 @@ __global__ void __launch_bounds__(256) merge_tc_kernel(const __half* __restrict_
 bool tc_supported(int H) { return H % tc::kHeads == 0; }
 bool tc_fp8_rows_supported(int) { return false; }
 
+namespace {
+
+// Per-device launch setup of the kernel: its shared-memory size, and for
+// every cluster size S how many clusters of S CTAs can be resident at once
+// (0: S cannot be launched).
+struct TcDevice {
+  bool ready = false;
+  int max_active[tc::kMaxCluster + 1] = {0};
+};
+TcDevice g_tc_dev[64];
+
+int tc_prepare() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+  TcDevice& d = g_tc_dev[dev];
+  if (d.ready) return dev;
+  cudaError_t e = cudaFuncSetAttribute(tc::decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       tc::kSmemBytes);
+  if (e != cudaSuccess) return -1;
+  const bool non_portable =
+      cudaFuncSetAttribute(tc::decode_tc_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+  for (int s = 1; s <= tc::kMaxCluster; ++s) {
+    d.max_active[s] = 0;
+    if (s > 8 && !non_portable) continue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(s, 1, 1);
+    cfg.blockDim = dim3(tc::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = tc::kSmemBytes;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = s;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, tc::decode_tc_kernel, &cfg) == cudaSuccess) d.max_active[s] = n;
+  }
+  cudaGetLastError();  // a refused cluster size leaves no sticky error
+  d.ready = true;
+  return dev;
+}
+
+}  // namespace
+
+int tc_max_splits() {
+  const int dev = tc_prepare();
+  if (dev < 0) return 8;  // no device: the portable cluster size
+  int s = tc::kMaxCluster;
+  while (s > 1 && g_tc_dev[dev].max_active[s] < 1) --s;
+  return s;
+}
+
+// Key splits per token: enough CTAs to fill the SMs, at most as many
+// clusters as can be resident at once, then the fewest splits that give the
+// busiest CTA the same number of tiles.
 int tc_default_splits(int T, int H, int topk, int num_sms) {
   const int tiles = (topk + tc::kTile - 1) / tc::kTile;
-  const int ctas_per_split = T * (H / tc::kHeads);
-  int s = num_sms / max(1, ctas_per_split);
+  const int clusters = T * (H / tc::kHeads);
+  int s = num_sms / max(1, clusters);
   if (s < 1) s = 1;
   if (s > tiles) s = tiles;
+  const int dev = tc_prepare();
+  if (dev < 0) {
+    if (s > 8) s = 8;
+  } else {
+    while (s > 1 && g_tc_dev[dev].max_active[s] < clusters) --s;
+  }
   const int per = (tiles + s - 1) / s;  // tiles of the busiest CTA
   return (tiles + per - 1) / per;       // fewest splits with that load
 }
 
 size_t tc_workspace_bytes(int T, int H, int splits) {
   if (splits <= 1) return 0;
-  return static_cast<size_t>(T) * splits * H * (kLatent * sizeof(__half) + 2 * sizeof(float));
+  return static_cast<size_t>(T) * (H / tc::kHeads) * splits *
+         (tc::kHeads * kLatent * sizeof(__half) + tc::kHeads * 2 * sizeof(float));
 }
 
 cudaError_t launch_decode_tc(int fmt, const void* q_latent, const void* q_rope, const uint8_t* cache,
@@ -946,6 +1080,7 @@ cudaError_t launch_decode_tc(int fmt, const void* q_latent, const void* q_rope, 
                              cudaStream_t stream) {
   if (fmt != 0) return cudaErrorNotSupported;
   (void)row_idx;
+  if (tc_prepare() < 0) return cudaErrorInvalidDevice;
   tc::Params p;
   p.q_latent = static_cast<const __nv_bfloat16*>(q_latent);
   p.q_rope = static_cast<const __nv_bfloat16*>(q_rope);
@@ -957,25 +1092,26 @@ cudaError_t launch_decode_tc(int fmt, const void* q_latent, const void* q_rope, 
   p.sl2 = sm_scale * kLog2e;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lse = lse;
+  p.ws_o16 = static_cast<__half*>(workspace);
+  p.ws_ml = splits > 1 ? reinterpret_cast<float*>(p.ws_o16 + static_cast<size_t>(T) * (H / tc::kHeads) * splits *
+                                                                 tc::kHeads * kLatent)
+                       : nullptr;
   p.num_splits = splits;
   p.tiles_total = (topk + tc::kTile - 1) / tc::kTile;
-  p.ws_o16 = static_cast<__half*>(workspace);
-  p.ws_ml = splits > 1 ? reinterpret_cast<float*>(p.ws_o16 + static_cast<size_t>(T) * splits * H * kLatent) : nullptr;
   p.err_word = err_word;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(tc::decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         tc::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  dim3 grid(splits, T, H / tc::kHeads);
-  tc::decode_tc_kernel<<<grid, tc::kThreads, tc::kSmemBytes, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || splits == 1) return e;
-  tc::merge_tc_kernel<<<dim3(T, H / tc::kHeads, kLatent / tc::kMergeDims), 256, 0, stream>>>(p.ws_o16, p.ws_ml, splits,
-                                                                                              H, p.out, lse);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(splits, T, H / tc::kHeads);
+  cfg.blockDim = dim3(tc::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = tc::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = splits;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tc::decode_tc_kernel, p);
 }
 
 }  // namespace nvmla

@@ -190,7 +190,7 @@ def test_small_workspace_falls_back(lib, cuda, tiny_setup):
     parity.assert_close(out, lse, ro, rl, "fallback")
 
 
-@pytest.mark.parametrize("splits", [1, 2, 3, 16])
+@pytest.mark.parametrize("splits", [1, 2, 3, 5, 8, 16])
 def test_tcgen05_splits(lib, cuda, splits):
     """The tcgen05 kernel with explicit key splits (single CTA per token up to
     one CTA per 128-row tile), on the decode-point shape with fewer tokens."""
@@ -200,9 +200,15 @@ def test_tcgen05_splits(lib, cuda, splits):
     ro, rl, _ = parity.oracle_decode(w, ref_cache)
     err = torch.zeros(2, dtype=torch.int32, device=cuda)
     d = parity.device_inputs(w, cuda)
-    out, lse = lib.sparse_mla_decode(d["q_latent"], d["q_rope"], cache, d["block_table"], d["topk_idx"], w.sm_scale,
-                                     q_seq_idx=d["q_seq_idx"], seq_lens=d["seq_lens"], err_word=err,
-                                     impl=lib.IMPL_TCGEN05, num_splits=splits)
+    try:
+        out, lse = lib.sparse_mla_decode(d["q_latent"], d["q_rope"], cache, d["block_table"], d["topk_idx"],
+                                         w.sm_scale, q_seq_idx=d["q_seq_idx"], seq_lens=d["seq_lens"], err_word=err,
+                                         impl=lib.IMPL_TCGEN05, num_splits=splits)
+    except lib.NvmlaError as e:
+        # more than 8 CTAs per cluster is a device option
+        if splits > 8 and e.status == 2 and "cluster" in str(e):
+            pytest.skip(str(e))
+        raise
     parity.assert_close(out, lse, ro, rl, f"tcgen05 splits={splits}")
     assert err.cpu().tolist() == [0, 0]
 
