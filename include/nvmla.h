@@ -45,7 +45,7 @@
  *   - nvmla_last_error() describes the most recent failing call of the
  *     calling thread.
  *
- * Cache layout (device, uint8 [num_pages][64][352], 16-byte aligned):
+ * Cache layout (device, uint8 [num_pages][64][352], 32-byte aligned):
  *   row = 256 code bytes | 32 scale bytes | 64 RoPE bytes  [Serving, "Making
  *   room for low-latency decode": 512 values at 4 bits with one FP8 scale per
  *   16 values, 64 RoPE values kept in FP8, 352 bytes per row].
@@ -102,7 +102,7 @@ typedef enum {
  *   slot_mapping  (device) int32 [n_tokens] physical slot of each token;
  *                 a negative slot skips the token; a slot >= num_pages*64 is
  *                 skipped and flagged NVMLA_ERRW_PACK_SLOT.
- *   cache         (device) uint8 [num_pages][64][352], 16-byte aligned.
+ *   cache         (device) uint8 [num_pages][64][352], 32-byte aligned.
  *   err_word      (device, nullable) see above.
  *
  * Per group of 16 values: amax = max |v|; scale byte = E4M3(amax / 6), round
@@ -127,7 +127,7 @@ nvmla_status nvfp4_mla_pack(const void* latent_bf16, int64_t latent_stride,
  *
  *   q_latent     (device) bf16 [T][H][512] contiguous, 16-byte aligned.
  *   q_rope       (device) bf16 [T][H][64] contiguous, 16-byte aligned.
- *   cache        (device) uint8 [num_pages][64][352], 16-byte aligned.
+ *   cache        (device) uint8 [num_pages][64][352], 32-byte aligned.
  *   block_table  (device) int32 [num_seqs][max_pages_per_seq].
  *   topk_idx     (device) int32 [T][topk] logical positions; -1 = empty slot.
  *   q_seq_idx    (device, nullable) int32 [T] sequence of each token (NULL:

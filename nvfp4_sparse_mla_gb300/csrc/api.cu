@@ -99,7 +99,7 @@ nvmla_status check_queries(const void* q_latent, const void* q_rope, const void*
 nvmla_status check_cache(const uint8_t* cache, int64_t num_pages, const int32_t* block_table, int32_t num_seqs,
                          int32_t max_pages, const int32_t* topk_idx) {
   if (!cache || !block_table || !topk_idx) return fail(NVMLA_ERR_INVALID_ARG, "null cache/block_table/topk_idx");
-  if (!aligned(cache, 16)) return fail(NVMLA_ERR_INVALID_ARG, "cache must be 16-byte aligned");
+  if (!aligned(cache, 32)) return fail(NVMLA_ERR_INVALID_ARG, "cache must be 32-byte aligned");
   if (num_pages < 1) return fail(NVMLA_ERR_INVALID_ARG, "num_pages = %lld must be >= 1", (long long)num_pages);
   if (num_pages * NVMLA_PAGE_TOKENS >= (int64_t{1} << 31)) return fail(NVMLA_ERR_UNSUPPORTED, "cache has 2^31 slots or more");
   if (num_seqs < 1 || max_pages < 1) return fail(NVMLA_ERR_INVALID_ARG, "num_seqs and max_pages_per_seq must be >= 1");
@@ -201,7 +201,7 @@ nvmla_status nvfp4_mla_pack(const void* latent_bf16, int64_t latent_stride, cons
   if (!aligned(rope_bf16, 4) || rope_stride < NVMLA_ROPE_DIM || rope_stride % 2 != 0)
     return fail(NVMLA_ERR_INVALID_ARG, "rope must be 4-byte aligned with an even stride >= 64");
   if (!aligned(slot_mapping, 4)) return fail(NVMLA_ERR_INVALID_ARG, "slot_mapping must be 4-byte aligned");
-  if (!aligned(cache, 16)) return fail(NVMLA_ERR_INVALID_ARG, "cache must be 16-byte aligned");
+  if (!aligned(cache, 32)) return fail(NVMLA_ERR_INVALID_ARG, "cache must be 32-byte aligned");
   if (num_pages < 1) return fail(NVMLA_ERR_INVALID_ARG, "num_pages must be >= 1");
   if (err_word && !aligned(err_word, 4)) return fail(NVMLA_ERR_INVALID_ARG, "err_word must be 4-byte aligned");
   return counted(launch_pack(latent_bf16, latent_stride, rope_bf16, rope_stride, slot_mapping, n_tokens, cache,
@@ -248,7 +248,8 @@ nvmla_status sparse_mla_decode_ex(const void* q_latent, const void* q_rope, cons
   if (err_word && !aligned(err_word, 4)) return fail(NVMLA_ERR_INVALID_ARG, "err_word must be 4-byte aligned");
   if (opts && (opts->impl < 0 || opts->impl > NVMLA_IMPL_TCGEN05 || opts->num_splits < 0))
     return fail(NVMLA_ERR_INVALID_ARG, "bad options");
-  RowSelect sel{topk_idx, block_table, q_seq_idx, seq_lens, num_pages * NVMLA_PAGE_TOKENS, topk, max_pages_per_seq};
+  RowSelect sel{topk_idx, block_table, q_seq_idx, seq_lens, num_pages * NVMLA_PAGE_TOKENS, topk, max_pages_per_seq,
+                num_seqs};
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int impl = pick_impl(opts, H);
   if (impl == NVMLA_IMPL_TCGEN05 && !tc_supported(H))
@@ -287,7 +288,8 @@ nvmla_status nvfp4_stage_dequant_fp8(const uint8_t* cache, int64_t num_pages, co
   if (!fp8_rows || !row_idx) return fail(NVMLA_ERR_INVALID_ARG, "null fp8_rows/row_idx");
   if (!aligned(fp8_rows, 16) || !aligned(row_idx, 4)) return fail(NVMLA_ERR_INVALID_ARG, "fp8_rows must be 16-byte aligned");
   if (err_word && !aligned(err_word, 4)) return fail(NVMLA_ERR_INVALID_ARG, "err_word must be 4-byte aligned");
-  RowSelect sel{topk_idx, block_table, q_seq_idx, seq_lens, num_pages * NVMLA_PAGE_TOKENS, topk, max_pages_per_seq};
+  RowSelect sel{topk_idx, block_table, q_seq_idx, seq_lens, num_pages * NVMLA_PAGE_TOKENS, topk, max_pages_per_seq,
+                num_seqs};
   return counted(launch_stage_dequant(cache, sel, T, fp8_rows, row_idx, err_word, reinterpret_cast<cudaStream_t>(stream)),
                  1, "nvfp4_stage_dequant_fp8 launch");
 }

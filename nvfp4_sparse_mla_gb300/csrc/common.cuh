@@ -102,6 +102,7 @@ __device__ __forceinline__ void report_error(int32_t* err_word, int32_t flag, in
 
 // Physical cache slot of slot k of query token t, or -1 (padding or a bad
 // entry; bad entries are reported once, by the caller's choice of thread).
+// A token whose sequence index lies outside [0, num_seqs) has no valid slot.
 struct RowSelect {
   const int32_t* topk_idx;
   const int32_t* block_table;
@@ -110,11 +111,16 @@ struct RowSelect {
   int64_t num_slots;
   int32_t topk;
   int32_t max_pages;
+  int32_t num_seqs;
 
   __device__ __forceinline__ int64_t slot(int t, int k, int32_t* err_word, bool report) const {
     const int32_t p = __ldg(topk_idx + static_cast<int64_t>(t) * topk + k);
     if (p == -1) return -1;
     const int32_t b = q_seq_idx ? __ldg(q_seq_idx + t) : 0;
+    if (b < 0 || b >= num_seqs) {
+      if (report) report_error(err_word, NVMLA_ERRW_BAD_INDEX, 1);
+      return -1;
+    }
     int64_t limit = static_cast<int64_t>(max_pages) * kPage;
     if (seq_lens) {
       const int64_t L = __ldg(seq_lens + b);

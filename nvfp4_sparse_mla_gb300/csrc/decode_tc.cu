@@ -5,54 +5,64 @@
 // query token only the rows the indexer selected are loaded, unpacked on chip
 // and attended to with FP16 operands and FP32 accumulation, with no FP8
 // staging buffer in GPU memory; the token's selected rows are divided among a
-// cluster of cooperating CTAs whose partial results are combined through
-// distributed shared memory in the same launch. "Prime Intellect unveils
-// Prime Inference", section "4-bit caches open the way": item 1 (one warp
-// group unpacks rows while others compute scores and accumulate), item 3
-// (empty slots of the 2048-slot list contribute nothing).
+// cluster of cooperating CTAs whose partial results are combined in the same
+// launch. "Prime Intellect unveils Prime Inference", section "4-bit caches
+// open the way": item 1 (one warp group unpacks rows while others compute
+// scores and accumulate), item 3 (empty slots of the 2048-slot list
+// contribute nothing).
 //
 // One cluster = one query token x 64 heads; its S CTAs take contiguous
-// ranges of the token's slots, in tiles of 128 rows. Roles in a CTA:
+// ranges of the token's slots, in tiles of 128 rows. Roles in a CTA
+// (17 warps):
 //
-//   warps 0-7  unpack: thread (row r, part h) loads the parts of its cache
-//              row it needs (192 of the 352 bytes) straight into registers
-//              and writes fp16 operands (E2M1 x E4M3 is exact in fp16) into
-//              shared memory, 128B-swizzled: latent chunk c = 2j + h (64
-//              dims) for j = 0..3 and half of the RoPE chunk. Each piece of
-//              the next tile's row is requested as soon as the current tile
-//              no longer needs its registers.
-//   MMA issue: one softmax thread issues QK as chunk pairs land and PV as
-//              soon as P^T is written; M = 128 throughout:
-//                S^T[128 rows, 64 heads]   = K[128 x 576] . Q^T   (9 chunks)
-//                O^T[512 dims, 64 heads]  += V^T[512 x 128] . P^T (4 blocks)
-//              The latent chunks are unpacked once: a K-major 128-row x
-//              64-dim chunk is byte for byte the MN-major layout of V^T for
-//              those 64 value dims, so block j of PV reads chunks 2j, 2j+1.
-//              Block j's completion frees chunks 2j, 2j+1 for the next tile.
-//   warps 8-15 softmax: warp (lane quadrant q, head half g) owns TMEM lanes
-//              32q..32q+31 (= rows) and heads 32g..32g+31. The running
-//              maximum of every head stays fixed while no score exceeds it by
-//              more than 2^8 (P stays below 256, safe in fp16); only a tile
-//              that does (always the first) pays for the exact cross-row
-//              maximum and the rescale of O^T in TMEM. Row sums accumulate per
-//              thread and are reduced across rows once, at the end. P^T goes
-//              to shared memory in place of the RoPE chunk, which QK no
-//              longer needs.
+//   warps 0-7   unpack: thread (row r, half h) loads the half of its cache
+//               row it converts -- the 128 code bytes of latent dims
+//               256h..256h+255, their 16 scale bytes and RoPE values
+//               32h..32h+31 -- with six 32- / 16-byte loads (176 bytes), and
+//               writes fp16 operands (E2M1 x E4M3 is exact in fp16) into
+//               shared memory, 128B-swizzled: at step j latent chunk 4h + j
+//               (64 dims), then its half of the RoPE chunk. Each piece of the
+//               next tile's row is requested as soon as the current tile no
+//               longer needs its registers.
+//   warp 16     MMA issue (one thread) and TMEM allocation. M = 128 always:
+//                 S^T[128 rows, 64 heads]  = K[128 x 576] . Q^T   (9 chunks)
+//                 O^T[512 dims, 64 heads] += V^T[512 x 128] . P^T (4 blocks)
+//               QK of chunk pair (j, j + 4) starts as soon as step j of the
+//               unpack lands. The latent chunks are unpacked once: a K-major
+//               128-row x 64-dim chunk is byte for byte the MN-major layout
+//               of V^T for those 64 value dims, so PV block j reads chunks j
+//               and j + 4 (dims 64j.. and 256 + 64j..) and its completion
+//               frees exactly what step j of the next tile's unpack writes.
+//               A tcgen05.mma issue holds the issuing thread for about the
+//               instruction's run time, hence a warp of its own.
+//   warps 8-15  softmax: warp (lane quadrant q, head half g) owns TMEM lanes
+//               32q..32q+31 (= rows) and heads 32g..32g+31. The running
+//               maximum of every head stays fixed while no score exceeds it
+//               by more than 2^8 (P stays below 256, safe in fp16); only a
+//               tile that does (always the first) pays for the exact
+//               cross-row maximum and the rescale of O^T in TMEM. Row sums
+//               accumulate per thread and are reduced across rows once, at
+//               the end. P^T goes to shared memory in place of the RoPE
+//               chunk, which QK no longer needs.
 //
-// Start-up issues the dependent loads first (slot list -> block table ->
-// rows of the first tile; L2 prefetch of the later tiles' rows) and converts
-// the query block while they are in flight.
+// Start-up issues the dependent loads first (slot list and sequence ->
+// block table and sequence length -> rows of the first tile, three levels;
+// L2 prefetch of the later tiles' rows) and converts the query block while
+// they are in flight.
 //
 // Combine: a token's only CTA writes out / lse itself. With S CTAs, each
-// writes O / l (fp16) and its per-head (m, l) to the workspace (they stay in
-// L2); after one cluster barrier, CTA r weights the S partials of its share
-// of the 512 value dims by l_s 2^(m_s - M) / L (M, L over the cluster) and
-// writes bf16 out (rank 0 also writes lse). Distributed shared memory moves
-// 64 KB per CTA more slowly than this L2 round trip does on GB300.
+// normalises its O^T block by block as PV finishes (O / l, fp16, in the
+// freed latent chunk) and stores it to the workspace with TMA bulk copies,
+// plus its per-head (m, l); after one cluster barrier CTA r loads its share
+// of the 512 value dims from all S partials (TMA bulk loads into the freed
+// query block), weights them by l_s 2^(m_s - M) / L (M, L over the cluster)
+// and writes bf16 out (rank 0 also writes lse). On GB300 this round trip
+// through L2 moves a CTA's 64 KB partial faster than distributed shared
+// memory does.
 //
-// Shared memory: query block (72 KB, later the output staging buffer) +
-// latent tile (128 KB) + RoPE/P^T chunk (16 KB, later the combine weights) +
-// slot list. TMEM: S^T 64 columns, O^T 4 x 64 columns.
+// Shared memory: query block (72 KB) + slot list (8 KB), later the combine's
+// receive buffer; latent tile (128 KB), later the partial staging; RoPE/P^T
+// chunk (16 KB), later the combine weights. TMEM: S^T 64 columns, O^T 4 x 64.
 // Every mbarrier wait is bounded: on timeout the CTA sets
 // NVMLA_ERRW_WAIT_TIMEOUT, drains its MMAs and still takes part in the
 // cluster barrier, so that every CTA of the cluster exits.
@@ -76,7 +86,6 @@ __device__ unsigned long long nvmla_tc_trace[kTraceCtas][kTracePoints];
       unsigned long long t_;                                                                         \
       asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t_));                                          \
       nvmla_tc_trace[cta_][(id)] = t_;                                                               \
-      if ((id) == 0 || (id) == 34) nvmla_tc_trace[cta_][120 + ((id) == 34)] = clock64();             \
     }                                                                                                \
   } while (0)
 #else
@@ -85,47 +94,72 @@ __device__ unsigned long long nvmla_tc_trace[kTraceCtas][kTracePoints];
   } while (0)
 #endif
 
-constexpr int kTile = 128;           // rows per tile (MMA M)
-constexpr int kHeads = 64;           // heads per CTA (MMA N)
-constexpr int kMaxTiles = 16;        // 2048 slots
-constexpr int kThreads = 512;        // 16 warps: 4 per SM sub-partition
-constexpr int kUnpackThreads = 256;  // warps 0-7
-constexpr int kSoftmaxWarp0 = 8;     // warps 8-15; thread 256 also issues every MMA
-constexpr int kAllocWarp = 9;        // allocates and frees TMEM
-constexpr int kMaxCluster = 16;      // CTAs sharing one token
-constexpr int kChunkBytes = 16384;   // 128 rows x 128 bytes
-constexpr int kPieces = 12;          // 16-byte pieces of a row one unpack thread holds
+constexpr int kTile = 128;              // rows per tile (MMA M)
+constexpr int kHeads = 64;              // heads per CTA (MMA N)
+constexpr int kMaxTiles = 16;           // 2048 slots
+constexpr int kUnpackThreads = 256;     // warps 0-7
+constexpr int kSoftmax0 = 256;          // warps 8-15: threads 256..511
+constexpr int kMmaWarp = 16;            // issues every MMA; allocates TMEM
+constexpr int kThreads = 544;           // 17 warps
+constexpr int kMaxCluster = 16;         // CTAs sharing one token
+constexpr int kChunkBytes = 16384;      // 128 rows x 128 bytes
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;        // S^T: columns [0, 64)
-constexpr uint32_t kColO = 64;       // O^T block j: columns [64 + 64 j, +64)
-constexpr float kTau = 8.0f;         // rescale threshold, log2 units
+constexpr uint32_t kColS = 0;           // S^T: columns [0, 64)
+constexpr uint32_t kColO = 64;          // O^T block j: columns [64 + 64 j, +64)
+constexpr uint32_t kColK = 320;         // K ring: kRing slots of 32 columns (64 fp16 dims x 128 rows)
+constexpr int kRing = 6;                // a tile's 9 K chunks: batch A = chunk uses 0-5 in slots 0-5,
+                                        // batch B = uses 6-8 in slots 0-2
+static_assert(kColK + 32 * kRing <= kTmemCols, "TMEM budget");
+constexpr float kTau = 8.0f;            // rescale threshold, log2 units
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
+constexpr int kPartBytes = kLatent * kHeads * 2;  // one CTA's fp16 partial: 64 KB
+constexpr int kMlBytes = kHeads * 8;              // its per-head (m, l)
 
 // shared memory map (bytes); the base is 1 KB aligned
-constexpr int kOffQ = 0;                              // 9 x 8 KB: query, K-major; later output staging
-constexpr int kOffL = kOffQ + 9 * 8192;               // 8 x 16 KB: latent tile; later the fp16 partial
-constexpr int kOffR = kOffL + 8 * kChunkBytes;        // 16 KB: RoPE chunk, then P^T
-constexpr int kOffSlots = kOffR + kChunkBytes;        // kMaxTiles x 128 int32
-constexpr int kOffRed = kOffSlots + kMaxTiles * kTile * 4;  // 4 quadrants x 64 heads fp32
-constexpr int kOffM = kOffRed + 4 * kHeads * 4;       // 64 fp32 running maxima (log2 units)
-constexpr int kOffAlpha = kOffM + kHeads * 4;         // 64 fp32 rescale factors, later combine weights
-constexpr int kOffMl = kOffAlpha + kHeads * 4;        // 64 x (m, l) published to the cluster
-constexpr int kOffBar = kOffMl + kHeads * 8;
+constexpr int kOffQ = 0;                               // 9 x 8 KB: query, K-major
+constexpr int kOffSlots = kOffQ + 9 * 8192;            // kMaxTiles x 128 int32
+constexpr int kRxBytes = kOffSlots + kMaxTiles * kTile * 4;  // query + slots: combine receive buffer
+constexpr int kOffL = kRxBytes;                        // 8 x 16 KB: V (latent) tile, later partial staging
+constexpr int kOffR = kOffL + 8 * kChunkBytes;         // 16 KB: P^T, then the combine weights
+constexpr int kOffRed = kOffR + kChunkBytes;           // 4 quadrants x 64 heads fp32
+constexpr int kOffM = kOffRed + 4 * kHeads * 4;        // 64 fp32 running maxima (log2 units)
+constexpr int kOffAlpha = kOffM + kHeads * 4;          // 64 fp32 rescale factors, later 1 / l
+constexpr int kOffMl = kOffAlpha + kHeads * 4;         // 64 x (m, l) of this CTA
+constexpr int kOffBar = kOffMl + kMlBytes;
 enum Bar {
-  kBarPairFull = 0,  // 4: latent chunks 2j, 2j+1 written (8 unpack warps)
-  kBarRopeFull = 4,  // RoPE chunk written (8 unpack warps)
-  kBarLFree = 5,     // 4: PV block j done -> chunks 2j, 2j+1 reusable (commit)
-  kBarRFree = 9,     // PV done -> RoPE/P^T chunk reusable (commit)
-  kBarSFull = 10,    // QK done (commit)
-  kBarPFull = 11,    // P^T written and O^T rescaled (8 softmax warps)
-  kBarODone = 12,    // PV done (commit)
-  kBarDrain = 13,    // every MMA finished (commit)
-  kNumBars = 14
+  // Few barriers on purpose: a wait or a branch between tcgen05.mma
+  // instructions stalls the issuing thread for about as long as several
+  // MMAs, so the issuer waits once per batch of MMAs.
+  kBarKFullA = 0,    // K chunks 0-5 of a tile in the ring (8 unpack warps) and S^T of the
+                     // previous tile read (8 softmax warps)
+  kBarKFreeA = 1,    // QK batch A done -> ring slots 0-2 reusable (commit)
+  kBarKFullB = 2,    // K chunks 6-8 in ring slots 0-2 (8 unpack warps)
+  kBarQKDone = 3,    // QK done: S^T full, every ring slot reusable (commit)
+  kBarPVReady = 4,   // P^T written (8 softmax warps) and V written (8 unpack warps)
+  kBarPVDone = 5,    // PV done: V tile and P^T buffer reusable, O^T settled (commit)
+  kBarDrain = 6,     // every MMA finished (commit)
+  kBarRx = 7,        // combine: the S partial slices have landed (TMA)
+  kBarQ = 8,         // the raw query block has landed (TMA)
+  kBarLastPV = 9,    // 4: block j of the last tile's PV done (commit)
+  kNumBars = 13
 };
 constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
 constexpr int kSmemBytes = kOffMisc + 16;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(kHeads * kLatent * 2 <= 9 * 8192, "output staging fits the query region");
+static_assert(kOffL % 1024 == 0 && kOffR % 1024 == 0, "swizzled operands need 1 KB alignment");
+static_assert(kOffMl % 16 == 0, "bulk copy source alignment");
+
+// value dims [dim_lo(r), dim_lo(r + 1)) are combined by CTA r of S
+__host__ __device__ constexpr int dim_lo(int r, int S) { return 4 * ((r * (kLatent / 4)) / S); }
+// receive buffer of the combine: S slices of D rows of 128 bytes, then S (m, l) blocks
+__host__ __device__ constexpr int rx_bytes(int D, int S) { return S * (D * 128 + kMlBytes); }
+constexpr bool rx_fits_every_split_count() {
+  for (int S = 2; S <= kMaxCluster; ++S)
+    for (int r = 0; r < S; ++r)
+      if (rx_bytes(dim_lo(r + 1, S) - dim_lo(r, S), S) > kRxBytes) return false;
+  return true;
+}
+static_assert(rx_fits_every_split_count(), "combine receive buffer");
 
 struct Params {
   const __nv_bfloat16* q_latent;
@@ -136,8 +170,8 @@ struct Params {
   float sl2;
   __nv_bfloat16* out;
   float* lse;
-  __half* ws_o16;   // [T][H / 64][S][8 head pieces][512][8 heads] partials O / l
-  float* ws_ml;     // [T][H / 64][S][64][2] (m in log2 units, l)
+  __half* ws_o16;  // [T][H / 64][S][512 dims][64 heads] partials O / l (16-byte units swizzled by dim)
+  float* ws_ml;    // [T][H / 64][S][64][2] (m in log2 units, l)
   int num_splits;  // == cluster size
   int tiles_total;
   int32_t* err_word;
@@ -151,6 +185,10 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -162,8 +200,16 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
 // try_wait that lets the hardware suspend the thread until the phase
-// completes or about `hint_ns` pass, so waiting warps take no issue slots
+// completes or about `hint_ns` pass, so that waiting warps neither take
+// issue slots nor hammer shared memory
 __device__ __forceinline__ bool mbar_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
   uint32_t ok;
   asm volatile(
@@ -176,21 +222,15 @@ __device__ __forceinline__ bool mbar_wait_hint(uint32_t bar, uint32_t parity, ui
   return ok != 0;
 }
 
-__device__ __forceinline__ uint64_t globaltimer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-  return t;
-}
-
-// Bounded wait for the phase with the given parity: try_wait suspends in
-// hardware until the phase completes or a short internal timeout; the loop
-// gives up after kWaitLimitNs of wall time, raising the CTA's abort flag and
-// NVMLA_ERRW_WAIT_TIMEOUT. Also returns false once another role aborted.
+// Bounded wait for the phase with the given parity: the thread sleeps in
+// try_wait until the phase completes; the loop gives up after kWaitLimitNs
+// of wall time, raising the CTA's abort flag and NVMLA_ERRW_WAIT_TIMEOUT.
+// Also returns false once another role aborted.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* err_word) {
   if (mbar_test(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    if (mbar_wait_hint(bar, parity, 20000)) return true;
+    if (mbar_wait_hint(bar, parity, 100000)) return true;
     if (*abort_flag) return false;
     if (globaltimer_ns() - t0 > kWaitLimitNs) break;
   }
@@ -205,14 +245,14 @@ __device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, vol
                                               int32_t* err_word) {
   bool ok = true;
   if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, abort_flag, err_word);
-  __syncwarp();  // orders the other lanes' later accesses after lane 0's acquire
+  __syncwarp();
   return __shfl_sync(0xffffffffu, ok, 0);
 }
 
 // Bounded wait without abort handling (drain paths).
 __device__ __forceinline__ void wait_bar_drain(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer_ns();
-  while (!mbar_wait_hint(bar, parity, 20000) && globaltimer_ns() - t0 < kWaitLimitNs) {
+  while (!mbar_test(bar, parity) && globaltimer_ns() - t0 < kWaitLimitNs) {
   }
 }
 
@@ -269,40 +309,10 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
         "=f"(r[o + 12]), "=f"(r[o + 13]), "=f"(r[o + 14]), "=f"(r[o + 15])                                    \
       : "r"(taddr))
 
-// 64 consecutive TMEM columns of this thread's lane, as fp32
-__device__ __forceinline__ void tmem_ld64f(uint32_t taddr, float (&r)[64]) {
-  NVMLA_TMEM_LD16F(taddr + 0, r, 0);
-  NVMLA_TMEM_LD16F(taddr + 16, r, 16);
-  NVMLA_TMEM_LD16F(taddr + 32, r, 32);
-  NVMLA_TMEM_LD16F(taddr + 48, r, 48);
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-// 64 consecutive TMEM columns of this thread's lane
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
-  NVMLA_TMEM_LD16(taddr + 0, r, 0);
-  NVMLA_TMEM_LD16(taddr + 16, r, 16);
-  NVMLA_TMEM_LD16(taddr + 32, r, 32);
-  NVMLA_TMEM_LD16(taddr + 48, r, 48);
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&r)[64]) {
-  NVMLA_TMEM_ST16(taddr + 0, r, 0);
-  NVMLA_TMEM_ST16(taddr + 16, r, 16);
-  NVMLA_TMEM_ST16(taddr + 32, r, 32);
-  NVMLA_TMEM_ST16(taddr + 48, r, 48);
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
 // 32 consecutive TMEM columns of this thread's lane
 __device__ __forceinline__ void tmem_ld32f(uint32_t taddr, float (&r)[32]) {
   NVMLA_TMEM_LD16F(taddr + 0, r, 0);
   NVMLA_TMEM_LD16F(taddr + 16, r, 16);
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-  NVMLA_TMEM_LD16(taddr + 0, r, 0);
-  NVMLA_TMEM_LD16(taddr + 16, r, 16);
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
@@ -341,7 +351,7 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
   return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
 }
 
-// ---- cluster: rank, and a barrier over every thread of every CTA with
+// ---- cluster rank and a barrier over every thread of every CTA with
 // release / acquire semantics at cluster scope
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
@@ -351,17 +361,20 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
-// L2-only loads (the data was written by other CTAs of the cluster)
-__device__ __forceinline__ uint4 ldg_cg_v4(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p) : "memory");
-  return v;
+
+// ---- TMA bulk copies (1-D): addresses 16-byte aligned, sizes multiples of 16
+__device__ __forceinline__ void bulk_store(void* gdst, uint32_t ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc), "r"(bytes)
+               : "memory");
 }
-__device__ __forceinline__ float2 ldg_cg_f2(const float* p) {
-  float2 v;
-  asm volatile("ld.global.cg.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p) : "memory");
-  return v;
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_load(uint32_t sdst, const void* gsrc, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(sdst),
+               "l"(gsrc), "r"(bytes), "r"(bar)
+               : "memory");
 }
+__device__ __forceinline__ void fence_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
 // fire-and-forget prefetch of a row into L2 (16-byte aligned, size a
 // multiple of 16)
@@ -369,18 +382,121 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
-// 16 E2M1 codes (8 bytes) times one scale -> two 16-byte fp16 chunks
-__device__ __forceinline__ void unpack16(uint32_t lo, uint32_t hi, uint32_t s2, uint4& a, uint4& b) {
-  uint32_t h[4];
-  e2m1x8_to_f16x8(lo, h);
-  a = make_uint4(hmul2_u32(h[0], s2), hmul2_u32(h[1], s2), hmul2_u32(h[2], s2), hmul2_u32(h[3], s2));
-  e2m1x8_to_f16x8(hi, h);
-  b = make_uint4(hmul2_u32(h[0], s2), hmul2_u32(h[1], s2), hmul2_u32(h[2], s2), hmul2_u32(h[3], s2));
+// ---- global loads (read-only path); the loads are volatile so that they
+// are issued where they stand, as soon as their registers are free, and not
+// sunk next to their first use
+__device__ __forceinline__ void ldg_nc_v8(const void* p, uint32_t* v) {
+  asm volatile("ld.global.nc.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+               : "l"(p));
+}
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ int32_t ldg_nc_s32(const int32_t* p) {
+  int32_t v;
+  asm volatile("ld.global.nc.s32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
 }
 
-__device__ __forceinline__ void zero_row(uint8_t* dst_base, int r) {
+// latent chunk of one row (64 dims) from its 32 code bytes and the 4 scale
+// bytes of its groups: 16-byte unit u holds dims 8u..8u+7 (group u / 2)
+__device__ __forceinline__ void write_chunk(const uint32_t (&c)[8], uint32_t scw, uint8_t* chunk, int r) {
 #pragma unroll
-  for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(dst_base + swz(r, c)) = make_uint4(0, 0, 0, 0);
+  for (int g = 0; g < 4; ++g) {
+    const uint32_t s2 = e4m3_to_f16x2_bcast((scw >> (8 * g)) & 0xffu);
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      uint32_t h[4];
+      e2m1x8_to_f16x8(c[2 * g + q], h);
+      *reinterpret_cast<uint4*>(chunk + swz(r, 2 * g + q)) =
+          make_uint4(hmul2_u32(h[0], s2), hmul2_u32(h[1], s2), hmul2_u32(h[2], s2), hmul2_u32(h[3], s2));
+    }
+  }
+}
+
+// RoPE values 32h .. 32h + 31 of one row (units 4h .. 4h + 3 of the chunk)
+__device__ __forceinline__ void write_rope(const uint32_t (&v)[8], int h, uint8_t* chunk, int r) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 a;
+    e4m3x4_to_f16x4(v[2 * q], a.x, a.y);
+    e4m3x4_to_f16x4(v[2 * q + 1], a.z, a.w);
+    *reinterpret_cast<uint4*>(chunk + swz(r, 4 * h + q)) = a;
+  }
+}
+
+// E2M1 -> fp16 as in e2m1x8_to_f16x8, for the K copy of a chunk. The
+// unused operand `salt` makes this a different expression from the V copy's
+// conversion, so that the compiler converts each copy at its own time
+// instead of keeping 128 converted registers alive between the two.
+__device__ __forceinline__ void e2m1x8_to_f16x8_k(uint32_t w, uint32_t salt, uint32_t (&h)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(w), "r"(salt));
+}
+
+// one row of a K chunk (64 dims = 32 columns of fp16 pairs) into this
+// thread's TMEM lane: column 4u + e holds dims 8u + 2e, 8u + 2e + 1
+__device__ __forceinline__ void tmem_store_chunk(const uint32_t (&c)[8], uint32_t scw, bool valid, uint32_t taddr,
+                                                 uint32_t salt) {
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    uint32_t w[16];
+#pragma unroll
+    for (int g2 = 0; g2 < 2; ++g2) {
+      const int g = 2 * half + g2;
+      const uint32_t s2 = e4m3_to_f16x2_bcast((scw >> (8 * g)) & 0xffu);
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        uint32_t h[4];
+        e2m1x8_to_f16x8_k(c[2 * g + q], salt, h);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) w[8 * g2 + 4 * q + e] = valid ? hmul2_u32(h[e], s2) : 0u;
+      }
+    }
+    NVMLA_TMEM_ST16(taddr + 16 * half, w, 0);
+  }
+}
+
+// the RoPE chunk of one row (64 E4M3 bytes -> 32 columns of fp16 pairs)
+__device__ __forceinline__ void tmem_store_rope(const uint32_t (&v)[16], bool valid, uint32_t taddr) {
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    uint32_t w[16];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      uint32_t lo, hi;
+      e4m3x4_to_f16x4(v[8 * half + q], lo, hi);
+      w[2 * q] = valid ? lo : 0u;
+      w[2 * q + 1] = valid ? hi : 0u;
+    }
+    NVMLA_TMEM_ST16(taddr + 16 * half, w, 0);
+  }
+}
+
+// QK MMA with A (the K rows) in TMEM and B (Q^T) in shared memory
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                           uint32_t accum) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accum)
+      : "memory");
+}
+
+__device__ __forceinline__ void zero_units(uint8_t* chunk, int r, int u0, int n) {
+#pragma unroll
+  for (int u = 0; u < 8; ++u)
+    if (u >= u0 && u < u0 + n) *reinterpret_cast<uint4*>(chunk + swz(r, u)) = make_uint4(0, 0, 0, 0);
 }
 
 // transposing butterfly: 32 values per lane -> lane L holds the reduction
@@ -400,72 +516,6 @@ __device__ __forceinline__ void warp_reduce32(float (&v)[32], int lane) {
       v[i] = kMax ? fmaxf(keep, recv) : keep + recv;
     }
   }
-}
-
-// The 16-byte pieces of a 352-byte row that unpack thread part h holds:
-// codes of latent chunks h, h+2, h+4, h+6 (pieces 2c, 2c+1), both scale
-// pieces (16, 17) and its half of the RoPE bytes (18 + 2h, 19 + 2h).
-__device__ __forceinline__ int piece_of(int n, int h) {
-  return n < 8 ? 2 * (2 * (n >> 1) + h) + (n & 1) : (n < 10 ? 16 + (n - 8) : 18 + 2 * h + (n - 10));
-}
-
-// latent chunk c = 2j + h of one row (64 dims) from the held pieces
-__device__ __forceinline__ void write_latent(const uint4 (&raw)[kPieces], int j, int h, uint8_t* chunk, int r) {
-  const uint4 c0 = raw[2 * j], c1 = raw[2 * j + 1];
-  const int c = 2 * j + h;
-  const uint4 sp = raw[8 + (c >> 2)];  // scale piece: groups 16*(c>>2) .. +15
-  const uint32_t sw = ((c & 3) == 0) ? sp.x : ((c & 3) == 1) ? sp.y : ((c & 3) == 2) ? sp.z : sp.w;
-  uint4 a, b;
-  unpack16(c0.x, c0.y, e4m3_to_f16x2_bcast(sw & 0xffu), a, b);
-  *reinterpret_cast<uint4*>(chunk + swz(r, 0)) = a;
-  *reinterpret_cast<uint4*>(chunk + swz(r, 1)) = b;
-  unpack16(c0.z, c0.w, e4m3_to_f16x2_bcast((sw >> 8) & 0xffu), a, b);
-  *reinterpret_cast<uint4*>(chunk + swz(r, 2)) = a;
-  *reinterpret_cast<uint4*>(chunk + swz(r, 3)) = b;
-  unpack16(c1.x, c1.y, e4m3_to_f16x2_bcast((sw >> 16) & 0xffu), a, b);
-  *reinterpret_cast<uint4*>(chunk + swz(r, 4)) = a;
-  *reinterpret_cast<uint4*>(chunk + swz(r, 5)) = b;
-  unpack16(c1.z, c1.w, e4m3_to_f16x2_bcast(sw >> 24), a, b);
-  *reinterpret_cast<uint4*>(chunk + swz(r, 6)) = a;
-  *reinterpret_cast<uint4*>(chunk + swz(r, 7)) = b;
-}
-
-// RoPE values 32h .. 32h + 31 of one row
-__device__ __forceinline__ void write_rope(const uint4 (&raw)[kPieces], int h, uint8_t* chunk, int r) {
-#pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    const uint4 v = raw[10 + q];
-    uint4 a, b;
-    e4m3x4_to_f16x4(v.x, a.x, a.y);
-    e4m3x4_to_f16x4(v.y, a.z, a.w);
-    e4m3x4_to_f16x4(v.z, b.x, b.y);
-    e4m3x4_to_f16x4(v.w, b.z, b.w);
-    *reinterpret_cast<uint4*>(chunk + swz(r, 4 * h + 2 * q)) = a;
-    *reinterpret_cast<uint4*>(chunk + swz(r, 4 * h + 2 * q + 1)) = b;
-  }
-}
-
-__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
-  return v;
-}
-__device__ __forceinline__ int32_t ldg_nc_s32(const int32_t* p) {
-  int32_t v;
-  asm volatile("ld.global.nc.s32 %0, [%1];" : "=r"(v) : "l"(p));
-  return v;
-}
-
-// Held pieces n0 .. n1-1 of the row in slot `slot` (nothing for a masked
-// slot). The loads are volatile so that they are issued here, as soon as the
-// registers are free, and not sunk next to their first use.
-__device__ __forceinline__ void load_pieces(const uint8_t* cache, int32_t slot, int h, uint4 (&raw)[kPieces], int n0,
-                                            int n1) {
-  if (slot < 0) return;
-  const uint8_t* row = cache + static_cast<int64_t>(slot) * kRowBytes;
-#pragma unroll
-  for (int n = 0; n < kPieces; ++n)
-    if (n >= n0 && n < n1) raw[n] = ldg_nc_v4(row + 16 * piece_of(n, h));
 }
 
 __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) {
@@ -492,245 +542,310 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
   const int nkeys = max(0, kend - kbeg);
   const int ntiles = (nkeys + kTile - 1) / kTile;  // <= kMaxTiles (host check)
 
-  if (tid == 0) NVMLA_TRACE_POINT(40);
+  if (tid == 0) NVMLA_TRACE_POINT(0);
 
-  // sequence facts of this token
-  const int32_t seq = p.sel.q_seq_idx ? __ldg(p.sel.q_seq_idx + t) : 0;
-  const int32_t* bt_row = p.sel.block_table + static_cast<int64_t>(seq) * p.sel.max_pages;
-  const int32_t* idx_row = p.sel.topk_idx + static_cast<int64_t>(t) * p.topk;
-  // slot of position pos (-1 for padding or a bad entry, which is reported
-  // when `report`)
-  auto slot_of_pos = [&](int32_t pos, int64_t limit, bool report) -> int32_t {
-    if (pos == -1) return -1;
-    if (pos < 0 || pos >= limit) {
-      if (report) report_error(p.err_word, NVMLA_ERRW_BAD_INDEX, 1);
-      return -1;
-    }
-    const int64_t page = __ldg(bt_row + (pos >> 6));
-    const int64_t s = page * kPage + (pos & 63);
-    if (page < 0 || s >= p.sel.num_slots) {
-      if (report) report_error(p.err_word, NVMLA_ERRW_BAD_SLOT, 1);
-      return -1;
-    }
-    return static_cast<int32_t>(s);
-  };
+  // ---- the query block (bf16, 64 KB latent + 8 KB RoPE, contiguous in
+  // global memory) is requested first, with two TMA bulk loads into the
+  // latent tile's space; it is converted after the barrier setup below
+  if (tid == 0) {
+    mbar_init(bar(kBarQ), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    fence_async_smem();
+    mbar_arrive_expect_tx(bar(kBarQ), kHeads * kDqk * 2);
+    const int64_t qh0 = static_cast<int64_t>(t) * p.H + h0;
+    bulk_load(sbase + kOffL, p.q_latent + qh0 * kLatent, kHeads * kLatent * 2, bar(kBarQ));
+    bulk_load(sbase + kOffL + kHeads * kLatent * 2, p.q_rope + qh0 * kRope, kHeads * kRope * 2, bar(kBarQ));
+  }
 
-  // ---- start-up: the dependent loads first (slot list, block table, rows),
-  // the query block while they are in flight
+  // ---- start-up, level 1: the token's sequence and slot-list entries
   const bool is_unpack = tid < kUnpackThreads;
-  const int ur = tid & 127, uh = (tid >> 7) & 1;  // unpack threads: row, part
-  const int sj = tid - kUnpackThreads;            // softmax threads: 0..255
-  uint4 raw[kPieces];
-  int32_t slot0 = -1;
+  const bool is_softmax = tid >= kSoftmax0 && tid < kSoftmax0 + 256;
+  const int ur = tid & 127, uh = (tid >> 7) & 1;  // unpack threads: row, half
+  const int sj = tid - kSoftmax0;                 // softmax threads: 0..255
+  const int32_t seq_raw = p.sel.q_seq_idx ? ldg_nc_s32(p.sel.q_seq_idx + t) : 0;
   int32_t pos0 = -1;
   constexpr int kLaterPer = kMaxTiles / 2;  // later tiles per softmax thread
   int32_t posl[kLaterPer];
   if (is_unpack) {
-    if (kbeg + ur < kend) pos0 = ldg_nc_s32(idx_row + kbeg + ur);
-  } else {
+    if (kbeg + ur < kend) pos0 = ldg_nc_s32(p.sel.topk_idx + static_cast<int64_t>(t) * p.topk + kbeg + ur);
+  } else if (is_softmax) {
     // softmax thread sj handles row sj % 128 of tiles 1 + sj / 128 + 2m
 #pragma unroll
     for (int m = 0; m < kLaterPer; ++m) {
       const int i = 1 + (sj >> 7) + 2 * m;
       const int key = kbeg + i * kTile + (sj & 127);
-      posl[m] = (i < ntiles && key < kend) ? ldg_nc_s32(idx_row + key) : -1;
+      posl[m] = (i < ntiles && key < kend) ? ldg_nc_s32(p.sel.topk_idx + static_cast<int64_t>(t) * p.topk + key) : -1;
     }
   }
-  constexpr int kQPer = kHeads * 72 / kThreads;  // 9 query pieces per thread
-  uint4 qv[kQPer];
+  // ---- level 2: block-table entries (page index clamped into the row, so
+  // the load is in bounds whatever the entry) and the sequence length
+  const bool seq_ok = seq_raw >= 0 && seq_raw < p.sel.num_seqs;
+  const int32_t seq = seq_ok ? seq_raw : 0;
+  const int32_t* bt_row = p.sel.block_table + static_cast<int64_t>(seq) * p.sel.max_pages;
+  auto page_of = [&](int32_t pos) -> int32_t {
+    const int32_t pi = min(max(pos >> 6, 0), p.sel.max_pages - 1);
+    return ldg_nc_s32(bt_row + pi);
+  };
+  const bool report = blockIdx.z == 0;  // one head block reports bad entries
+  // slot of position pos given its block-table entry (-1 for padding or a
+  // bad entry, which is reported when `rep`)
+  auto classify = [&](int32_t pos, int32_t page, int64_t limit, bool rep) -> int32_t {
+    if (pos == -1) return -1;
+    if (!seq_ok || pos < 0 || pos >= limit) {
+      if (rep) report_error(p.err_word, NVMLA_ERRW_BAD_INDEX, 1);
+      return -1;
+    }
+    const int64_t s = static_cast<int64_t>(page) * kPage + (pos & 63);
+    if (page < 0 || s >= p.sel.num_slots) {
+      if (rep) report_error(p.err_word, NVMLA_ERRW_BAD_SLOT, 1);
+      return -1;
+    }
+    return static_cast<int32_t>(s);
+  };
+  int32_t page0 = 0;
+  int32_t pagel[kLaterPer];
+  if (is_unpack) {
+    page0 = page_of(pos0);
+  } else if (is_softmax) {
 #pragma unroll
-  for (int n = 0; n < kQPer; ++n) {
-    const int i = tid + kThreads * n;
-    const int h = i / 72, j = i % 72;
-    const int64_t qh = static_cast<int64_t>(t) * p.H + h0 + h;
-    qv[n] = j < 64 ? ldg_nc_v4(p.q_latent + qh * kLatent + 8 * j) : ldg_nc_v4(p.q_rope + qh * kRope + 8 * (j - 64));
+    for (int m = 0; m < kLaterPer; ++m) pagel[m] = (1 + (sj >> 7) + 2 * m < ntiles) ? page_of(posl[m]) : 0;
   }
   int64_t limit = static_cast<int64_t>(p.sel.max_pages) * kPage;
   if (p.sel.seq_lens) {
-    const int64_t L = __ldg(p.sel.seq_lens + seq);
+    const int64_t L = ldg_nc_s32(p.sel.seq_lens + seq);
     limit = L < limit ? L : limit;
   }
-  const bool report = blockIdx.z == 0;  // one head block reports bad entries
+
+  // ---- level 3: rows of the first tile (unpack threads, into registers),
+  // L2 prefetch of the later tiles' rows (softmax threads)
+  uint32_t rc[4][8];  // code bytes of latent chunks 4uh + j
+  uint4 rs;           // scale bytes of groups 16uh .. 16uh + 15
+  uint32_t rr[16];    // the 64 RoPE bytes (half 0 only)
+  int32_t slot0 = -1;
+  auto load_codes = [&](int32_t slot, int j) {
+    if (slot >= 0) ldg_nc_v8(p.cache + static_cast<int64_t>(slot) * kRowBytes + 128 * uh + 32 * j, rc[j]);
+  };
+  auto load_scale_rope = [&](int32_t slot) {
+    if (slot >= 0) {
+      const uint8_t* row = p.cache + static_cast<int64_t>(slot) * kRowBytes;
+      rs = ldg_nc_v4(row + kScaleOff + 16 * uh);
+      if (uh == 0) {
+        ldg_nc_v8(row + kRopeOff, rr);
+        ldg_nc_v8(row + kRopeOff + 32, rr + 8);
+      }
+    }
+  };
   if (is_unpack) {
-    if (ntiles > 0 && kbeg + ur < kend) slot0 = slot_of_pos(pos0, limit, report && uh == 0);
-    load_pieces(p.cache, slot0, uh, raw, 0, kPieces);
+    if (ntiles > 0 && kbeg + ur < kend) slot0 = classify(pos0, page0, limit, report && uh == 0);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) load_codes(slot0, j);
+    load_scale_rope(slot0);
     if (uh == 0) slots[ur] = slot0;
-  } else {
+  } else if (is_softmax) {
 #pragma unroll
     for (int m = 0; m < kLaterPer; ++m) {
       const int i = 1 + (sj >> 7) + 2 * m;
       if (i < ntiles) {
-        const int32_t s = slot_of_pos(posl[m], limit, report);
+        const int32_t s = classify(posl[m], pagel[m], limit, report);
         slots[i * kTile + (sj & 127)] = s;
         if (s >= 0) prefetch_l2(p.cache + static_cast<int64_t>(s) * kRowBytes, kRowBytes);
       }
     }
   }
-  if (tid == 0) NVMLA_TRACE_POINT(41);
+  if (tid == 0) NVMLA_TRACE_POINT(1);
 
-  // ---- setup
+  // ---- setup: barriers, TMEM, the query block
   if (tid == kThreads - 1) {
-    for (int j = 0; j < 4; ++j) {
-      mbar_init(bar(kBarPairFull + j), 8);
-      mbar_init(bar(kBarLFree + j), 1);
-    }
-    mbar_init(bar(kBarRopeFull), 8);
-    mbar_init(bar(kBarRFree), 1);
-    mbar_init(bar(kBarSFull), 1);
-    mbar_init(bar(kBarPFull), 8);
-    mbar_init(bar(kBarODone), 1);
+    mbar_init(bar(kBarKFullA), 16);
+    mbar_init(bar(kBarKFreeA), 1);
+    mbar_init(bar(kBarKFullB), 8);
+    mbar_init(bar(kBarQKDone), 1);
+    mbar_init(bar(kBarPVReady), 16);
+    mbar_init(bar(kBarPVDone), 1);
     mbar_init(bar(kBarDrain), 1);
+    mbar_init(bar(kBarRx), 1);
+    for (int j = 0; j < 4; ++j) mbar_init(bar(kBarLastPV + j), 1);
     *abort_flag = (sbase & 1023u) ? 1 : 0;  // swizzled operands need a 1 KB aligned base
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (tid < kHeads) m_run[tid] = -INFINITY;
-  if (warp == kAllocWarp) {
+  if (warp == kMmaWarp) {
+    __syncwarp();
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                  "r"(kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  }
-  // query block -> fp16, K-major 128B-swizzled (all 16 warps)
-#pragma unroll
-  for (int n = 0; n < kQPer; ++n) {
-    const int i = tid + kThreads * n;
-    const int h = i / 72, j = i % 72, c = j >> 3, q = j & 7;
-    const uint32_t w[4] = {qv[n].x, qv[n].y, qv[n].z, qv[n].w};
-    uint32_t o[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) o[e] = pack_f16x2(bf16_bits_to_f32(w[e] & 0xffffu), bf16_bits_to_f32(w[e] >> 16));
-    *reinterpret_cast<uint4*>(smem + kOffQ + c * 8192 + swz(h, q)) = make_uint4(o[0], o[1], o[2], o[3]);
   }
   fence_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // query block -> fp16, K-major 128B-swizzled (4608 pieces of 16 bytes);
+  // then the latent tile's space is free for the unpack
+  if (wait_bar_warp(bar(kBarQ), 0, abort_flag, p.err_word)) {
+    const uint8_t* qraw = smem + kOffL;
+    for (int i = tid; i < kHeads * 72; i += kThreads) {
+      const int h = i / 72, j = i % 72, c = j >> 3, q = j & 7;
+      const uint4 v = *reinterpret_cast<const uint4*>(
+          qraw + (j < 64 ? h * (kLatent * 2) + 16 * j : kHeads * kLatent * 2 + h * (kRope * 2) + 16 * (j - 64)));
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[e] = pack_f16x2(bf16_bits_to_f32(w[e] & 0xffffu), bf16_bits_to_f32(w[e] >> 16));
+      *reinterpret_cast<uint4*>(smem + kOffQ + c * 8192 + swz(h, q)) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+  fence_async_smem();
+  __syncthreads();
   if (*abort_flag && tid == 0) report_error(p.err_word, NVMLA_ERRW_WAIT_TIMEOUT, 1);
-  if (tid == 0) NVMLA_TRACE_POINT(0);
+  if (tid == 0) NVMLA_TRACE_POINT(2);
 
-  // roles; the softmax group's epilogue ends with the (m, l) of every head
-  // published in ml_pub
-  const int sw = warp - kSoftmaxWarp0;       // softmax warp 0..7
-  const int quad = sw & 3, hh = sw >> 2;     // TMEM lane quadrant, head half
-  const int hb = hh * 32;                    // first head of this thread
+  const int sw = warp - 8;                    // softmax warp 0..7
+  const int quad = sw & 3, hh = sw >> 2;      // TMEM lane quadrant, head half
+  const int hb = hh * 32;                     // first head of this thread
   const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+  const int64_t cbase = (static_cast<int64_t>(t) * gridDim.z + blockIdx.z) * S;  // first split of this cluster
   bool ok = true;
   if (is_unpack) {
     // ------------------------------------------------------------ unpack
+    // Chunk use u of a tile (u = 0..8): latent chunk 4 (u & 1) + u / 2 for
+    // u < 8, the RoPE chunk for u = 8; half uh writes the uses of parity uh
+    // (and half 0 the RoPE chunk). Uses 0-5 sit in ring slots 0-5 (batch A),
+    // uses 6-8 in slots 0-2 (batch B).
     ok = *abort_flag == 0;
     int32_t cur_slot = slot0;
+    const uint32_t krow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + kColK;  // this row's lane
     for (int i = 0; i < ntiles && ok; ++i) {
       const bool valid = cur_slot >= 0;
       const int32_t nxt_slot = (i + 1 < ntiles) ? slots[(i + 1) * kTile + ur] : -1;
-      if (tid == 0 && i < 2) {
-        uint32_t x = raw[0].x ^ raw[11].w;  // first use: the pieces have arrived
-        asm volatile("" ::"r"(x));
-        NVMLA_TRACE_POINT(44 + i);
-      }
-      for (int j = 0; j < 4 && ok; ++j) {
-        if (i >= 1) ok = wait_bar_warp(bar(kBarLFree + j), (i - 1) & 1, abort_flag, p.err_word);
-        if (!ok) break;
-        uint8_t* chunk = smem + kOffL + (2 * j + uh) * kChunkBytes;
-        if (valid) {
-          write_latent(raw, j, uh, chunk, ur);
-        } else {
-          zero_row(chunk, ur);
-        }
-        fence_async_smem();
-        warp_arrive(bar(kBarPairFull + j), lane);
-        // the registers of this pair (and of a scale piece once its last
-        // pair is written) now take the next tile's row
-        load_pieces(p.cache, nxt_slot, uh, raw, 2 * j, 2 * j + 2);
-        if (j == 1) load_pieces(p.cache, nxt_slot, uh, raw, 8, 9);
-        if (j == 3) load_pieces(p.cache, nxt_slot, uh, raw, 9, 10);
-      }
-      if (ok && i >= 1) ok = wait_bar_warp(bar(kBarRFree), (i - 1) & 1, abort_flag, p.err_word);
+      const uint32_t sc[4] = {rs.x, rs.y, rs.z, rs.w};
+      // K batch A: latent chunks 4uh + 0..2 -> slots uh, 2 + uh, 4 + uh
+      if (i >= 1) ok = wait_bar_warp(bar(kBarQKDone), (i - 1) & 1, abort_flag, p.err_word);
       if (!ok) break;
-      uint8_t* rc = smem + kOffR;
-      if (valid) {
-        write_rope(raw, uh, rc, ur);
-      } else {
+      tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(rc + swz(ur, 4 * uh + c)) = make_uint4(0, 0, 0, 0);
+      for (int j = 0; j < 3; ++j) tmem_store_chunk(rc[j], sc[j], valid, krow + 32 * (2 * j + uh), i);
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      tc_fence_before();
+      warp_arrive(bar(kBarKFullA), lane);
+      if (tid == 0 && i < 2) NVMLA_TRACE_POINT(10 + 4 * i);
+      // K batch B: latent chunk 4uh + 3 -> slot uh; the RoPE chunk (half 0) -> slot 2
+      ok = wait_bar_warp(bar(kBarKFreeA), i & 1, abort_flag, p.err_word);
+      if (!ok) break;
+      tc_fence_after();
+      tmem_store_chunk(rc[3], sc[3], valid, krow + 32 * uh, i);
+      if (uh == 0) tmem_store_rope(rr, valid, krow + 64);
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      tc_fence_before();
+      warp_arrive(bar(kBarKFullB), lane);
+      if (tid == 0 && i < 2) NVMLA_TRACE_POINT(11 + 4 * i);
+      // V (latent chunks 4uh + j) once PV of the previous tile has released
+      // the buffer; then these registers take the next tile's row
+      if (i >= 1) ok = wait_bar_warp(bar(kBarPVDone), (i - 1) & 1, abort_flag, p.err_word);
+      if (!ok) break;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint8_t* chunk = smem + kOffL + (4 * uh + j) * kChunkBytes;
+        if (valid) {
+          write_chunk(rc[j], sc[j], chunk, ur);
+        } else {
+          zero_units(chunk, ur, 0, 8);
+        }
+        load_codes(nxt_slot, j);
       }
       fence_async_smem();
-      warp_arrive(bar(kBarRopeFull), lane);
-      load_pieces(p.cache, nxt_slot, uh, raw, 10, 12);
+      warp_arrive(bar(kBarPVReady), lane);
+      load_scale_rope(nxt_slot);
       cur_slot = nxt_slot;
-      if (tid == 0 && i < 4) NVMLA_TRACE_POINT(14 + i);
+      if (tid == 0 && i < 2) NVMLA_TRACE_POINT(12 + 4 * i);
     }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issue
+    // Per tile: QK batch A (24 MMAs), PV of the previous tile (32), QK batch
+    // B (12); one wait before each batch, one commit after it. The softmax
+    // of a tile thus overlaps QK of the next.
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_f16(false, false);
+      constexpr uint32_t idesc_pv = idesc_f16(true, true);
+      const uint32_t lb = sbase + kOffL, rb = sbase + kOffR, qb = sbase + kOffQ;
+      const uint32_t ring = tmem + kColK;
+      bool mok = *abort_flag == 0;
+      // (the last tile's PV also reports each block, so that the epilogue
+      // can start on it)
+      auto issue_pv = [&](int i, bool last) {
+#pragma unroll 1
+        for (int j = 0; j < 4; ++j) {
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            mma_f16(tmem + kColO + 64 * j, sdesc(lb + j * kChunkBytes + 2048 * ks, 4 * kChunkBytes, 1024),
+                    sdesc(rb + 2048 * ks, 8192, 1024), idesc_pv, (i | ks) != 0);
+          if (last) mma_commit(bar(kBarLastPV + j));
+        }
+        mma_commit(bar(kBarPVDone));
+      };
+      for (int i = 0; i < ntiles && mok; ++i) {
+        mok = wait_bar(bar(kBarKFullA), i & 1, abort_flag, p.err_word);
+        if (!mok) break;
+        tc_fence_after();
+        // batch A: uses 0..5 (slot u, query chunk 4 (u & 1) + u / 2); loop
+        // back-edges, unlike conditional branches, cost the issue nothing
+#pragma unroll 1
+        for (int u = 0; u < 6; ++u) {
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            mma_f16_ts(tmem + kColS, ring + 32 * u + 8 * ks,
+                       sdesc(qb + (4 * (u & 1) + (u >> 1)) * 8192 + 32 * ks, 16, 1024), idesc_qk, (u | ks) != 0);
+        }
+        mma_commit(bar(kBarKFreeA));
+        if (i >= 1) {
+          mok = wait_bar(bar(kBarPVReady), (i - 1) & 1, abort_flag, p.err_word);
+          if (!mok) break;
+          tc_fence_after();
+          issue_pv(i - 1, false);
+        }
+        mok = wait_bar(bar(kBarKFullB), i & 1, abort_flag, p.err_word);
+        if (!mok) break;
+        tc_fence_after();
+        // batch B: uses 6, 7 (latent chunks 3, 7) in slots 0, 1; use 8 (RoPE) in slot 2
+#pragma unroll 1
+        for (int u = 0; u < 3; ++u) {
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            mma_f16_ts(tmem + kColS, ring + 32 * u + 8 * ks, sdesc(qb + (u == 2 ? 8 : 3 + 4 * u) * 8192 + 32 * ks, 16, 1024),
+                       idesc_qk, 1);
+        }
+        mma_commit(bar(kBarQKDone));
+      }
+      if (mok && ntiles > 0) {
+        mok = wait_bar(bar(kBarPVReady), (ntiles - 1) & 1, abort_flag, p.err_word);
+        if (mok) {
+          tc_fence_after();
+          issue_pv(ntiles - 1, true);
+        }
+      }
+      // every MMA issued has finished once this commit lands
+      mma_commit(bar(kBarDrain));
+      wait_bar_drain(bar(kBarDrain), 0);
+    }
+    __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
     const int k = quad * 32 + lane;  // row of this thread
-    const bool issuer = tid == kUnpackThreads;
-    constexpr uint32_t idesc_qk = idesc_f16(false, false);
-    constexpr uint32_t idesc_pv = idesc_f16(true, true);
-    const uint32_t lb = sbase + kOffL, rb = sbase + kOffR, qb = sbase + kOffQ;
-    // QK of one tile, issued by one thread: latent chunk pairs as they land,
-    // then the RoPE chunk
-    auto issue_qk = [&](int i) -> bool {
-      const uint32_t par = i & 1;
-      for (int j = 0; j < 4; ++j) {
-        if (!wait_bar(bar(kBarPairFull + j), par, abort_flag, p.err_word)) return false;
-        tc_fence_after();
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int c = 2 * j + cc;
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            mma_f16(tmem + kColS, sdesc(lb + c * kChunkBytes + 32 * ks, 16, 1024),
-                    sdesc(qb + c * 8192 + 32 * ks, 16, 1024), idesc_qk, (c | ks) != 0);
-        }
-      }
-      if (!wait_bar(bar(kBarRopeFull), par, abort_flag, p.err_word)) return false;
-      tc_fence_after();
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        mma_f16(tmem + kColS, sdesc(rb + 32 * ks, 16, 1024), sdesc(qb + 8 * 8192 + 32 * ks, 16, 1024), idesc_qk, 1);
-      mma_commit(bar(kBarSFull));
-      if (i < 4) NVMLA_TRACE_POINT(5 + 2 * i);
-      return true;
-    };
-    // PV of one tile: block j reads latent chunks 2j, 2j+1 as V^T and P^T
-    // from R; its completion frees those chunks for the next tile
-    auto issue_pv = [&](int i) -> bool {
-      if (!wait_bar(bar(kBarPFull), i & 1, abort_flag, p.err_word)) return false;
-      tc_fence_after();
-      for (int j = 0; j < 4; ++j) {
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          mma_f16(tmem + kColO + 64 * j, sdesc(lb + 2 * j * kChunkBytes + 2048 * ks, kChunkBytes, 1024),
-                  sdesc(rb + 2048 * ks, 8192, 1024), idesc_pv, !(i == 0 && ks == 0));
-        mma_commit(bar(kBarLFree + j));
-      }
-      mma_commit(bar(kBarRFree));
-      mma_commit(bar(kBarODone));
-      if (i < 4) NVMLA_TRACE_POINT(6 + 2 * i);
-      return true;
-    };
-
     float lp[32];  // this row's share of its heads' sums
 #pragma unroll
     for (int h = 0; h < 32; ++h) lp[h] = 0.f;
+    // S^T is free for the first tile
+    warp_arrive(bar(kBarKFullA), lane);
     ok = !softmax_sync_or(*abort_flag != 0);
-    // the issuer's outcome is made uniform across its warp before any
-    // warp-collective operation
-    auto issued = [&](bool mine) -> bool { return __shfl_sync(0xffffffffu, mine, 0); };
     for (int i = 0; i < ntiles && ok; ++i) {
-      // a failed PV issue of the previous tile left the abort flag raised;
-      // the issuer then issues nothing more, and the OR below ends the loop
-      // for the whole group at once
-      bool okq = true;
-      if (issuer) okq = *abort_flag == 0 && issue_qk(i);
-      ok = issued(okq);
-      if (ok) ok = wait_bar_warp(bar(kBarSFull), i & 1, abort_flag, p.err_word);
+      ok = wait_bar_warp(bar(kBarQKDone), i & 1, abort_flag, p.err_word);
       if (softmax_sync_or(!ok)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      if (tid == 256 && i < 4) NVMLA_TRACE_POINT(21 + 3 * i);
+      if (tid == kSoftmax0 && i < 2) NVMLA_TRACE_POINT(30 + 3 * i);
       const bool valid = slots[i * kTile + k] >= 0;
       float s[32];
       tmem_ld32f(tmem + lane_base + kColS + hb, s);
@@ -743,8 +858,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
         for (int h = 0; h < 32; ++h) excess = fmaxf(excess, s[h] - m_run[hb + h]);
       }
       const bool slow = softmax_sync_or(excess > kTau);
-      if (slow) {
-        // exact per-head maximum of this tile (destroys s; reloaded below)
+      bool pv_done = i == 0;  // PV of the previous tile has finished
+      if (!slow) {
+        // S^T is in registers: QK of the next tile may overwrite it
+        tc_fence_before();
+        warp_arrive(bar(kBarKFullA), lane);
+      } else {
+        // exact per-head maximum of this tile (destroys s, reloaded below
+        // before S^T is released)
         warp_reduce32<true>(s, lane);
         red[quad * 64 + hb + lane] = s[0];
         softmax_sync();
@@ -759,27 +880,33 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
         softmax_sync();
 #pragma unroll
         for (int h = 0; h < 32; ++h) lp[h] *= alpha_s[hb + h];
-        if (i >= 1) {
-          // O^T holds the finished PV of the earlier tiles (QK of this tile
-          // could only start after the last of them); 16 columns at a time
-#pragma unroll 1
-          for (int jq = 0; jq < 8; ++jq) {
-            const uint32_t col = kColO + 64 * (jq >> 1) + hb + 16 * (jq & 1);
-            uint32_t orr[16];
-            NVMLA_TMEM_LD16(tmem + lane_base + col, orr, 0);
-            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-            const float* al = alpha_s + hb + 16 * (jq & 1);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * al[e]);
-            NVMLA_TMEM_ST16(tmem + lane_base + col, orr, 0);
-          }
-          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-        }
         tmem_ld32f(tmem + lane_base + kColS + hb, s);
 #pragma unroll
         for (int h = 0; h < 32; ++h) s[h] = valid ? s[h] * p.sl2 : -INFINITY;
+        tc_fence_before();
+        warp_arrive(bar(kBarKFullA), lane);
+        if (i >= 1) {
+          // O^T must hold the finished PV of every earlier tile
+          ok = wait_bar_warp(bar(kBarPVDone), (i - 1) & 1, abort_flag, p.err_word);
+          pv_done = true;
+          tc_fence_after();
+          if (ok) {
+            // 16 columns at a time
+#pragma unroll 1
+            for (int jq = 0; jq < 8; ++jq) {
+              const uint32_t col = kColO + 64 * (jq >> 1) + hb + 16 * (jq & 1);
+              uint32_t orr[16];
+              NVMLA_TMEM_LD16(tmem + lane_base + col, orr, 0);
+              asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+              const float* al = alpha_s + hb + 16 * (jq & 1);
+#pragma unroll
+              for (int e = 0; e < 16; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * al[e]);
+              NVMLA_TMEM_ST16(tmem + lane_base + col, orr, 0);
+            }
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+          }
+        }
       }
-      if (tid == 256 && i < 4) NVMLA_TRACE_POINT(22 + 3 * i);
       // P = 2^(s - m); masked rows give 0
 #pragma unroll
       for (int h = 0; h < 32; ++h) {
@@ -787,8 +914,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
         s[h] = pv;
         lp[h] += pv;
       }
-      // P^T row (this thread's 32 heads) -> the RoPE chunk's place (QK of
-      // this tile is complete)
+      // P^T row (this thread's 32 heads) -> R, once PV of the previous tile
+      // has read it
+      if (!pv_done) ok = wait_bar_warp(bar(kBarPVDone), (i - 1) & 1, abort_flag, p.err_word);
       uint8_t* pt = smem + kOffR;
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
@@ -801,194 +929,177 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
       }
       fence_async_smem();
       tc_fence_before();
-      warp_arrive(bar(kBarPFull), lane);
-      if (tid == 256 && i < 4) NVMLA_TRACE_POINT(23 + 3 * i);
-      if (issuer) issue_pv(i);
+      warp_arrive(bar(kBarPVReady), lane);
+      if (tid == kSoftmax0 && i < 2) NVMLA_TRACE_POINT(31 + 3 * i);
+      if (softmax_sync_or(!ok)) {
+        ok = false;
+        break;
+      }
     }
     // ------------------------------------------------------------ row sums
-    if (ok && ntiles > 0) ok = wait_bar_warp(bar(kBarODone), (ntiles - 1) & 1, abort_flag, p.err_word);
     ok = !softmax_sync_or(!ok);
-    tc_fence_after();
-    if (tid == 256) NVMLA_TRACE_POINT(33);
     warp_reduce32<false>(lp, lane);
     red[quad * 64 + hb + lane] = lp[0];
     softmax_sync();
     if (quad == 0) {
       const int h = hb + lane;
       const float l = (red[h] + red[64 + h]) + (red[128 + h] + red[192 + h]);
-      const bool live = ok && l > 0.f;
+      const bool live = ok && ntiles > 0 && l > 0.f;
       ml_pub[2 * h] = live ? m_run[h] : -INFINITY;
       ml_pub[2 * h + 1] = live ? l : 0.f;
       alpha_s[h] = live ? 1.f / l : 0.f;
+      if (S == 1) p.lse[static_cast<int64_t>(t) * p.H + h0 + h] = live ? (m_run[h] + log2f(l)) * kLn2 : -INFINITY;
     }
-    if (issuer) {
-      // every MMA issued has finished once this commit lands
-      mma_commit(bar(kBarDrain));
-      wait_bar_drain(bar(kBarDrain), 0);
-    }
-  }
-
-  // ------------------------------------------------------------ combine
-  if (S == 1) {
-    // the token's only CTA: O / l as bf16 [64 heads][512 dims] staged in the
-    // query block's place, then 16-byte stores of out
-    __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(smem + kOffQ);
-    __syncthreads();  // alpha_s (1 / l) of every head is written
-    if (!is_unpack) {
-#pragma unroll 1
-      for (int j = 0; j < 4; ++j) {
-        const int dv = 128 * j + quad * 32 + lane;
-        uint32_t o[32];
-        if (ok && ntiles > 0) {
-          tmem_ld32(tmem + lane_base + kColO + 64 * j + hb, o);
-        } else {
+    fence_async_smem();  // ml_pub is read by a bulk copy below
+    softmax_sync();
+    if (tid == kSoftmax0) NVMLA_TRACE_POINT(40);
+    // ------------------------------------------------------------ O^T, block by block as PV finishes
+    __half* wo = p.ws_o16 + (cbase + rank) * (kLatent * kHeads);
+    bool have = ok && ntiles > 0;
+    for (int j = 0; j < 4; ++j) {
+      if (have) have = wait_bar_warp(bar(kBarLastPV + j), 0, abort_flag, p.err_word);
+      tc_fence_after();
+      float o[32];
+      if (have) {
+        tmem_ld32f(tmem + lane_base + kColO + 64 * j + hb, o);
+      } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = 0u;
-        }
+        for (int e = 0; e < 32; ++e) o[e] = 0.f;
+      }
+      // TMEM lane k of block j: dim 64j + k (k < 64) or 256 + 64j + k - 64
+      const int d = (k < 64) ? 64 * j + k : 256 + 64 * j + (k - 64);
+      if (S == 1) {
 #pragma unroll
         for (int e = 0; e < 32; ++e)
-          stage[(hb + e) * kLatent + dv] = __float2bfloat16_rn(__uint_as_float(o[e]) * alpha_s[hb + e]);
-      }
-      tc_fence_before();
-      if (quad == 0) {
-        const int h = hb + lane;
-        const float m = ml_pub[2 * h], l = ml_pub[2 * h + 1];
-        p.lse[static_cast<int64_t>(t) * p.H + h0 + h] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
-      }
-    }
-    __syncthreads();
-    if (warp == kAllocWarp) {
-      tc_fence_after();
-      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
-    }
-#pragma unroll
-    for (int u = 0; u < kHeads * (kLatent / 8) / kThreads; ++u) {
-      const int pc = tid + kThreads * u, h = pc >> 6, g = pc & 63;
-      const uint4 v = *reinterpret_cast<const uint4*>(stage + h * kLatent + 8 * g);
-      *reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(t) * p.H + h0 + h) * kLatent + 8 * g) = v;
-    }
-  } else {
-    // S CTAs: each writes O / l (fp16, 8-head pieces x 512 dims) and its (m, l) to
-    // the workspace; after a cluster barrier CTA `rank` combines the S
-    // partials of its share [dv0, dv0 + ndv) of the value dims
-    const int64_t cbase = (static_cast<int64_t>(t) * gridDim.z + blockIdx.z) * S;  // first split of this cluster
-    __syncthreads();  // alpha_s (1 / l) of every head is written
-    if (!is_unpack) {
-      __half* wo = p.ws_o16 + (cbase + rank) * (kLatent * kHeads);
-#pragma unroll 1
-      for (int j = 0; j < 4; ++j) {
-        const int dv = 128 * j + quad * 32 + lane;
-        uint32_t o[32];
-        if (ok && ntiles > 0) {
-          tmem_ld32(tmem + lane_base + kColO + 64 * j + hb, o);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = 0u;
-        }
+          p.out[(static_cast<int64_t>(t) * p.H + h0 + hb + e) * kLatent + d] =
+              __float2bfloat16_rn(o[e] * alpha_s[hb + e]);
+      } else {
+        // normalised partial (fp16, [row k][64 heads], unit u of row k at
+        // u ^ (k & 7)) staged in latent chunk j, which PV no longer reads
+        uint8_t* stg = smem + kOffL + j * kChunkBytes + k * 128;
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
           uint32_t w4[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int hl = 8 * cc + 2 * e;
-            w4[e] = pack_f16x2(__uint_as_float(o[hl]) * alpha_s[hb + hl],
-                               __uint_as_float(o[hl + 1]) * alpha_s[hb + hl + 1]);
+            w4[e] = pack_f16x2(o[hl] * alpha_s[hb + hl], o[hl + 1] * alpha_s[hb + hl + 1]);
           }
-          // piece-major [8 head pieces][512 dims][8 heads]: a warp's lanes
-          // (consecutive dims) store 512 contiguous bytes
-          *reinterpret_cast<uint4*>(wo + ((4 * hh + cc) * kLatent + dv) * 8) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          *reinterpret_cast<uint4*>(stg + (((4 * hh + cc) ^ (k & 7)) << 4)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        }
+        fence_async_smem();
+        softmax_sync();
+        if (tid == kSoftmax0) {
+          const uint32_t src = sbase + kOffL + j * kChunkBytes;
+          bulk_store(wo + (64 * j) * kHeads, src, 64 * 128);
+          bulk_store(wo + (256 + 64 * j) * kHeads, src + 64 * 128, 64 * 128);
+          if (j == 3) bulk_store(p.ws_ml + (cbase + rank) * (kHeads * 2), sbase + kOffMl, kMlBytes);
+          bulk_commit();
+          if (j == 0) NVMLA_TRACE_POINT(47);
         }
       }
-      tc_fence_before();
-      if (quad == 0) {
-        const int h = hb + lane;
-        *reinterpret_cast<float2*>(p.ws_ml + ((cbase + rank) * kHeads + h) * 2) =
-            make_float2(ml_pub[2 * h], ml_pub[2 * h + 1]);
-      }
     }
+    tc_fence_before();
+    if (S > 1 && tid == kSoftmax0) {
+      // the partial is complete in global memory before the cluster barrier
+      bulk_wait_all();
+      fence_async_global();
+    }
+    if (tid == kSoftmax0) NVMLA_TRACE_POINT(41);
+  }
+
+  // ------------------------------------------------------------ combine
+  __syncthreads();  // every role is done with TMEM
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+  if (S > 1) {
     // release / acquire at cluster scope: every partial of the cluster is
     // visible to every CTA of it
     cluster_sync_all();
-    if (tid == 256) NVMLA_TRACE_POINT(35);
-    if (warp == kAllocWarp) {
-      tc_fence_after();
-      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
-    }
-    const int dv0 = 8 * ((static_cast<int>(rank) * (kLatent / 8)) / S);
-    const int ndv = 8 * (((static_cast<int>(rank) + 1) * (kLatent / 8)) / S) - dv0;
-    const int nitems = ndv * 8;  // (dim, 8-head piece)
-    const __half* wo0 = p.ws_o16 + cbase * (kLatent * kHeads);
-    uint4 v[8];
-    auto load_batch = [&](int item, int s0) {
-      const int piece = item / ndv, dl = item - piece * ndv;
-      const int64_t off = static_cast<int64_t>(piece * kLatent + dv0 + dl) * 8;
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        if (s0 + u < S) v[u] = ldg_cg_v4(wo0 + static_cast<int64_t>(s0 + u) * (kLatent * kHeads) + off);
-    };
-    // this thread's first partials are requested before the weights are known
-    if (tid < nitems) load_batch(tid, 0);
-    float* coef = reinterpret_cast<float*>(smem + kOffR);  // [S][64] combine weights
-    if (tid < kHeads) {
-      const int h = tid;
-      float2 ml[kMaxCluster];
-#pragma unroll
-      for (int s = 0; s < kMaxCluster; ++s)
-        if (s < S) ml[s] = ldg_cg_f2(p.ws_ml + ((cbase + s) * kHeads + h) * 2);
-      float M = -INFINITY;
-#pragma unroll
-      for (int s = 0; s < kMaxCluster; ++s)
-        if (s < S) M = fmaxf(M, ml[s].x);
-      float L = 0.f;
-#pragma unroll
-      for (int s = 0; s < kMaxCluster; ++s) {
-        if (s < S) {
-          const float w = ml[s].y > 0.f ? ml[s].y * ex2(ml[s].x - M) : 0.f;
-          ml[s].y = w;
-          L += w;
-        }
+    if (tid == 0) NVMLA_TRACE_POINT(42);
+    const int d0 = dim_lo(static_cast<int>(rank), S);
+    const int D = dim_lo(static_cast<int>(rank) + 1, S) - d0;
+    const uint32_t rx = sbase + kOffQ;
+    const uint32_t rx_ml = rx + S * D * 128;
+    if (tid == 0) {
+      fence_async_global();
+      mbar_arrive_expect_tx(bar(kBarRx), static_cast<uint32_t>(rx_bytes(D, S)));
+      for (int s = 0; s < S; ++s) {
+        bulk_load(rx + s * D * 128, p.ws_o16 + (cbase + s) * (kLatent * kHeads) + d0 * kHeads, D * 128, bar(kBarRx));
+        bulk_load(rx_ml + s * kMlBytes, p.ws_ml + (cbase + s) * (kHeads * 2), kMlBytes, bar(kBarRx));
       }
-      const float inv = L > 0.f ? 1.f / L : 0.f;
-#pragma unroll
-      for (int s = 0; s < kMaxCluster; ++s)
-        if (s < S) coef[s * kHeads + h] = ml[s].y * inv;
-      if (rank == 0) p.lse[static_cast<int64_t>(t) * p.H + h0 + h] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+      wait_bar(bar(kBarRx), 0, abort_flag, p.err_word);
     }
     __syncthreads();
-    if (tid == 256) NVMLA_TRACE_POINT(36);
-    __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(smem + kOffQ);  // [64 heads][ndv]
-    for (int it = tid; it < nitems; it += kThreads) {
-      const int piece = it / ndv, dl = it - piece * ndv;
+    if (tid == 0) NVMLA_TRACE_POINT(43);
+    // combine weights l_s 2^(m_s - M) / L per head, [S][64] in R: eight
+    // consecutive lanes per head, splits s = q, q + 8
+    float* coef = reinterpret_cast<float*>(smem + kOffR);
+    const float* rml = reinterpret_cast<const float*>(smem + kOffQ + S * D * 128);
+    if (tid < 8 * kHeads) {
+      const int h = tid >> 3, q = tid & 7;
+      float m2[2], l2[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int s = q + 8 * e;
+        l2[e] = s < S ? rml[s * 128 + 2 * h + 1] : 0.f;
+        m2[e] = l2[e] > 0.f ? rml[s * 128 + 2 * h] : -INFINITY;
+      }
+      float M = fmaxf(m2[0], m2[1]);
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      float w2[2], L = 0.f;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        w2[e] = l2[e] > 0.f ? l2[e] * ex2(m2[e] - M) : 0.f;
+        L += w2[e];
+      }
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+      const float inv = L > 0.f ? __frcp_rn(L) : 0.f;
+#pragma unroll
+      for (int e = 0; e < 2; ++e)
+        if (q + 8 * e < S) coef[(q + 8 * e) * kHeads + h] = w2[e] * inv;
+      if (rank == 0 && q == 0)
+        p.lse[static_cast<int64_t>(t) * p.H + h0 + h] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+    }
+    __syncthreads();
+    if (tid == 0) NVMLA_TRACE_POINT(45);
+    // item = (head group u, dim row dl): lanes take consecutive dims; the
+    // bf16 results go to [64 heads][D dims] in the latent tile's space (its
+    // bulk stores have completed), then to out in 8-byte pieces
+    const uint8_t* rxp = smem + kOffQ;
+    __nv_bfloat16* ostg = reinterpret_cast<__nv_bfloat16*>(smem + kOffL);
+    for (int it = tid; it < D * 8; it += kThreads) {
+      const int u = it / D, dl = it - u * D, d = d0 + dl;
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      for (int s0 = 0; s0 < S; s0 += 8) {
-        if (s0 > 0 || it != tid) load_batch(it, s0);
+#pragma unroll 4
+      for (int s = 0; s < S; ++s) {
+        const uint4 v = *reinterpret_cast<const uint4*>(rxp + s * D * 128 + dl * 128 + ((u ^ (d & 7)) << 4));
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        const float* c = coef + s * kHeads + 8 * u;
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          if (s0 + u < S) {
-            const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-            const float* c = coef + (s0 + u) * kHeads + 8 * piece;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
-              acc[2 * e] += c[2 * e] * f.x;
-              acc[2 * e + 1] += c[2 * e + 1] * f.y;
-            }
-          }
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+          acc[2 * e] += c[2 * e] * f.x;
+          acc[2 * e + 1] += c[2 * e + 1] * f.y;
         }
       }
 #pragma unroll
-      for (int e = 0; e < 8; ++e) stage[(8 * piece + e) * ndv + dl] = __float2bfloat16_rn(acc[e]);
+      for (int e = 0; e < 8; ++e) ostg[(8 * u + e) * D + dl] = __float2bfloat16_rn(acc[e]);
     }
     __syncthreads();
-    if (tid == 256) NVMLA_TRACE_POINT(38);
-    const int per_head = ndv / 8;
+    if (tid == 0) NVMLA_TRACE_POINT(46);
+    const int per_head = D / 4;
     for (int pc = tid; pc < kHeads * per_head; pc += kThreads) {
       const int h = pc / per_head, g = pc - h * per_head;
-      const uint4 w = *reinterpret_cast<const uint4*>(stage + h * ndv + 8 * g);
-      *reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(t) * p.H + h0 + h) * kLatent + dv0 + 8 * g) = w;
+      const uint2 v = *reinterpret_cast<const uint2*>(ostg + h * D + 4 * g);
+      *reinterpret_cast<uint2*>(p.out + (static_cast<int64_t>(t) * p.H + h0 + h) * kLatent + d0 + 4 * g) = v;
     }
   }
-  if (tid == 0) NVMLA_TRACE_POINT(34);
+  if (tid == 0) NVMLA_TRACE_POINT(44);
 }
 
 }  // namespace tc
@@ -1058,6 +1169,7 @@ int tc_default_splits(int T, int H, int topk, int num_sms) {
   int s = num_sms / max(1, clusters);
   if (s < 1) s = 1;
   if (s > tiles) s = tiles;
+  if (s > tc::kMaxCluster) s = tc::kMaxCluster;
   const int dev = tc_prepare();
   if (dev < 0) {
     if (s > 8) s = 8;
@@ -1070,8 +1182,7 @@ int tc_default_splits(int T, int H, int topk, int num_sms) {
 
 size_t tc_workspace_bytes(int T, int H, int splits) {
   if (splits <= 1) return 0;
-  return static_cast<size_t>(T) * (H / tc::kHeads) * splits *
-         (tc::kHeads * kLatent * sizeof(__half) + tc::kHeads * 2 * sizeof(float));
+  return static_cast<size_t>(T) * (H / tc::kHeads) * splits * (tc::kPartBytes + tc::kMlBytes);
 }
 
 cudaError_t launch_decode_tc(int fmt, const void* q_latent, const void* q_rope, const uint8_t* cache,
@@ -1081,6 +1192,7 @@ cudaError_t launch_decode_tc(int fmt, const void* q_latent, const void* q_rope, 
   if (fmt != 0) return cudaErrorNotSupported;
   (void)row_idx;
   if (tc_prepare() < 0) return cudaErrorInvalidDevice;
+  if (splits < 1 || splits > tc::kMaxCluster) return cudaErrorInvalidValue;
   tc::Params p;
   p.q_latent = static_cast<const __nv_bfloat16*>(q_latent);
   p.q_rope = static_cast<const __nv_bfloat16*>(q_rope);
