@@ -625,21 +625,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
   auto load_codes = [&](int32_t slot, int j) {
     if (slot >= 0) ldg_nc_v8(p.cache + static_cast<int64_t>(slot) * kRowBytes + 128 * uh + 32 * j, rc[j]);
   };
-  auto load_scale_rope = [&](int32_t slot) {
-    if (slot >= 0) {
+  auto load_scale = [&](int32_t slot) {
+    if (slot >= 0) rs = ldg_nc_v4(p.cache + static_cast<int64_t>(slot) * kRowBytes + kScaleOff + 16 * uh);
+  };
+  auto load_rope = [&](int32_t slot) {
+    if (slot >= 0 && uh == 0) {
       const uint8_t* row = p.cache + static_cast<int64_t>(slot) * kRowBytes;
-      rs = ldg_nc_v4(row + kScaleOff + 16 * uh);
-      if (uh == 0) {
-        ldg_nc_v8(row + kRopeOff, rr);
-        ldg_nc_v8(row + kRopeOff + 32, rr + 8);
-      }
+      ldg_nc_v8(row + kRopeOff, rr);
+      ldg_nc_v8(row + kRopeOff + 32, rr + 8);
     }
   };
   if (is_unpack) {
     if (ntiles > 0 && kbeg + ur < kend) slot0 = classify(pos0, page0, limit, report && uh == 0);
 #pragma unroll
     for (int j = 0; j < 4; ++j) load_codes(slot0, j);
-    load_scale_rope(slot0);
+    load_scale(slot0);
     if (uh == 0) slots[ur] = slot0;
   } else if (is_softmax) {
 #pragma unroll
@@ -730,7 +730,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
       tc_fence_before();
       warp_arrive(bar(kBarKFullA), lane);
       if (tid == 0 && i < 2) NVMLA_TRACE_POINT(10 + 4 * i);
-      // K batch B: latent chunk 4uh + 3 -> slot uh; the RoPE chunk (half 0) -> slot 2
+      // K batch B: latent chunk 4uh + 3 -> slot uh; the RoPE chunk (half 0) -> slot 2;
+      // the RoPE bytes are requested now, their latency hidden by the wait
+      load_rope(cur_slot);
       ok = wait_bar_warp(bar(kBarKFreeA), i & 1, abort_flag, p.err_word);
       if (!ok) break;
       tc_fence_after();
@@ -756,7 +758,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
       }
       fence_async_smem();
       warp_arrive(bar(kBarPVReady), lane);
-      load_scale_rope(nxt_slot);
+      load_scale(nxt_slot);
       cur_slot = nxt_slot;
       if (tid == 0 && i < 2) NVMLA_TRACE_POINT(12 + 4 * i);
     }
@@ -855,7 +857,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
       float excess = -INFINITY;
       if (valid) {
 #pragma unroll
-        for (int h = 0; h < 32; ++h) excess = fmaxf(excess, s[h] - m_run[hb + h]);
+        for (int h4 = 0; h4 < 8; ++h4) {
+          const float4 m4 = *reinterpret_cast<const float4*>(m_run + hb + 4 * h4);
+          excess = fmaxf(excess, fmaxf(fmaxf(s[4 * h4] - m4.x, s[4 * h4 + 1] - m4.y),
+                                       fmaxf(s[4 * h4 + 2] - m4.z, s[4 * h4 + 3] - m4.w)));
+        }
       }
       const bool slow = softmax_sync_or(excess > kTau);
       bool pv_done = i == 0;  // PV of the previous tile has finished
@@ -879,7 +885,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
         }
         softmax_sync();
 #pragma unroll
-        for (int h = 0; h < 32; ++h) lp[h] *= alpha_s[hb + h];
+        for (int h4 = 0; h4 < 8; ++h4) {
+          const float4 a4 = *reinterpret_cast<const float4*>(alpha_s + hb + 4 * h4);
+          lp[4 * h4] *= a4.x;
+          lp[4 * h4 + 1] *= a4.y;
+          lp[4 * h4 + 2] *= a4.z;
+          lp[4 * h4 + 3] *= a4.w;
+        }
         tmem_ld32f(tmem + lane_base + kColS + hb, s);
 #pragma unroll
         for (int h = 0; h < 32; ++h) s[h] = valid ? s[h] * p.sl2 : -INFINITY;
@@ -909,10 +921,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
       }
       // P = 2^(s - m); masked rows give 0
 #pragma unroll
-      for (int h = 0; h < 32; ++h) {
-        const float pv = valid ? ex2(s[h] - m_run[hb + h]) : 0.f;
-        s[h] = pv;
-        lp[h] += pv;
+      for (int h4 = 0; h4 < 8; ++h4) {
+        const float4 m4 = *reinterpret_cast<const float4*>(m_run + hb + 4 * h4);
+        const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int h = 4 * h4 + e;
+          const float pv = valid ? ex2(s[h] - mm[e]) : 0.f;
+          s[h] = pv;
+          lp[h] += pv;
+        }
       }
       // P^T row (this thread's 32 heads) -> R, once PV of the previous tile
       // has read it
