@@ -141,7 +141,8 @@ enum Bar {
   kBarRx = 7,        // combine: the S partial slices have landed (TMA)
   kBarQ = 8,         // the raw query block has landed (TMA)
   kBarLastPV = 9,    // 4: block j of the last tile's PV done (commit)
-  kNumBars = 13
+  kBarRxMl = 13,     // combine: the S (m, l) blocks have landed (TMA)
+  kNumBars = 14
 };
 constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
 constexpr int kSmemBytes = kOffMisc + 16;
@@ -664,6 +665,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
     mbar_init(bar(kBarPVDone), 1);
     mbar_init(bar(kBarDrain), 1);
     mbar_init(bar(kBarRx), 1);
+    mbar_init(bar(kBarRxMl), 1);
     for (int j = 0; j < 4; ++j) mbar_init(bar(kBarLastPV + j), 1);
     *abort_flag = (sbase & 1023u) ? 1 : 0;  // swizzled operands need a 1 KB aligned base
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -774,15 +776,26 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
       const uint32_t ring = tmem + kColK;
       bool mok = *abort_flag == 0;
       // (the last tile's PV also reports each block, so that the epilogue
-      // can start on it)
-      auto issue_pv = [&](int i, bool last) {
+      // can start on it; two straight-line copies, as a conditional branch
+      // between MMAs costs the issue)
+      auto issue_pv = [&](int i) {
 #pragma unroll 1
         for (int j = 0; j < 4; ++j) {
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
             mma_f16(tmem + kColO + 64 * j, sdesc(lb + j * kChunkBytes + 2048 * ks, 4 * kChunkBytes, 1024),
                     sdesc(rb + 2048 * ks, 8192, 1024), idesc_pv, (i | ks) != 0);
-          if (last) mma_commit(bar(kBarLastPV + j));
+        }
+        mma_commit(bar(kBarPVDone));
+      };
+      auto issue_pv_last = [&](int i) {
+#pragma unroll 1
+        for (int j = 0; j < 4; ++j) {
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            mma_f16(tmem + kColO + 64 * j, sdesc(lb + j * kChunkBytes + 2048 * ks, 4 * kChunkBytes, 1024),
+                    sdesc(rb + 2048 * ks, 8192, 1024), idesc_pv, (i | ks) != 0);
+          mma_commit(bar(kBarLastPV + j));
         }
         mma_commit(bar(kBarPVDone));
       };
@@ -804,7 +817,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
           mok = wait_bar(bar(kBarPVReady), (i - 1) & 1, abort_flag, p.err_word);
           if (!mok) break;
           tc_fence_after();
-          issue_pv(i - 1, false);
+          issue_pv(i - 1);
         }
         mok = wait_bar(bar(kBarKFullB), i & 1, abort_flag, p.err_word);
         if (!mok) break;
@@ -823,7 +836,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
         mok = wait_bar(bar(kBarPVReady), (ntiles - 1) & 1, abort_flag, p.err_word);
         if (mok) {
           tc_fence_after();
-          issue_pv(ntiles - 1, true);
+          issue_pv_last(ntiles - 1);
         }
       }
       // every MMA issued has finished once this commit lands
@@ -1042,21 +1055,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
     const uint32_t rx = sbase + kOffQ;
     const uint32_t rx_ml = rx + S * D * 128;
     if (tid == 0) {
+      // the small (m, l) blocks first: the weights are computed while the
+      // partial slices are still on their way
       fence_async_global();
-      mbar_arrive_expect_tx(bar(kBarRx), static_cast<uint32_t>(rx_bytes(D, S)));
-      for (int s = 0; s < S; ++s) {
+      mbar_arrive_expect_tx(bar(kBarRxMl), static_cast<uint32_t>(S * kMlBytes));
+      for (int s = 0; s < S; ++s)
+        bulk_load(rx_ml + s * kMlBytes, p.ws_ml + (cbase + s) * (kHeads * 2), kMlBytes, bar(kBarRxMl));
+      mbar_arrive_expect_tx(bar(kBarRx), static_cast<uint32_t>(S * D * 128));
+      for (int s = 0; s < S; ++s)
         bulk_load(rx + s * D * 128, p.ws_o16 + (cbase + s) * (kLatent * kHeads) + d0 * kHeads, D * 128, bar(kBarRx));
-        bulk_load(rx_ml + s * kMlBytes, p.ws_ml + (cbase + s) * (kHeads * 2), kMlBytes, bar(kBarRx));
-      }
-      wait_bar(bar(kBarRx), 0, abort_flag, p.err_word);
     }
-    __syncthreads();
-    if (tid == 0) NVMLA_TRACE_POINT(43);
     // combine weights l_s 2^(m_s - M) / L per head, [S][64] in R: eight
     // consecutive lanes per head, splits s = q, q + 8
     float* coef = reinterpret_cast<float*>(smem + kOffR);
     const float* rml = reinterpret_cast<const float*>(smem + kOffQ + S * D * 128);
-    if (tid < 8 * kHeads) {
+    if (tid < 8 * kHeads && wait_bar_warp(bar(kBarRxMl), 0, abort_flag, p.err_word)) {
       const int h = tid >> 3, q = tid & 7;
       float m2[2], l2[2];
 #pragma unroll
@@ -1083,8 +1096,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
       if (rank == 0 && q == 0)
         p.lse[static_cast<int64_t>(t) * p.H + h0 + h] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
     }
-    __syncthreads();
     if (tid == 0) NVMLA_TRACE_POINT(45);
+    wait_bar_warp(bar(kBarRx), 0, abort_flag, p.err_word);
+    __syncthreads();
+    if (tid == 0) NVMLA_TRACE_POINT(43);
     // item = (head group u, dim row dl): lanes take consecutive dims; the
     // bf16 results go to [64 heads][D dims] in the latent tile's space (its
     // bulk stores have completed), then to out in 8-byte pieces
@@ -1097,7 +1112,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
       for (int s = 0; s < S; ++s) {
         const uint4 v = *reinterpret_cast<const uint4*>(rxp + s * D * 128 + dl * 128 + ((u ^ (d & 7)) << 4));
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        const float* c = coef + s * kHeads + 8 * u;
+        const float4 c0 = *reinterpret_cast<const float4*>(coef + s * kHeads + 8 * u);
+        const float4 c1 = *reinterpret_cast<const float4*>(coef + s * kHeads + 8 * u + 4);
+        const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
