@@ -348,30 +348,52 @@ def main():
         dec_us, step_mean = float(t[0]), float(t[1])
 
     # ---------------- end to end through the public API with host buffers
-    h_ql = w.q_latent.pin_memory()
-    h_qr = w.q_rope.pin_memory()
-    h_tk = w.topk_idx.pin_memory()
-    h_nl, h_nr, h_ns = new_lat.pin_memory(), new_rope.pin_memory(), new_slots.pin_memory()
-    h_out = torch.empty((w.T, w.H, 512), dtype=torch.bfloat16).pin_memory()
-    h_lse = torch.empty((w.T, w.H), dtype=torch.float32).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (h_ql, h_qr, h_tk, h_nl, h_nr, h_ns))
-    d2h = h_out.numel() * 2 + h_lse.numel() * 4
+    # Every per-step input (queries, index lists, the new tokens) lives in
+    # one pinned host buffer and goes up with one copy; out and lse come back
+    # with one copy. The library calls take views of the device mirrors.
+    def packed(parts, align=256):
+        offs, total = [], 0
+        for t in parts:
+            offs.append(total)
+            total += (t.numel() * t.element_size() + align - 1) // align * align
+        return offs, total
+
+    in_parts = [w.q_latent, w.q_rope, w.topk_idx, new_lat, new_rope, new_slots]
+    in_offs, in_total = packed(in_parts)
+    h_in = torch.zeros(in_total, dtype=torch.uint8).pin_memory()
+    for t, o in zip(in_parts, in_offs):
+        n = t.numel() * t.element_size()
+        h_in[o:o + n].copy_(t.contiguous().view(-1).view(torch.uint8))
+    d_in = torch.empty(in_total, dtype=torch.uint8, device=dev)
+
+    def view(buf, off, like):
+        n = like.numel() * like.element_size()
+        return buf[off:off + n].view(like.dtype).view(like.shape)
+
+    d_ql, d_qr, d_tk, d_nl, d_nr, d_ns = (view(d_in, o, t) for t, o in zip(in_parts, in_offs))
+    out_like = torch.empty((w.T, w.H, 512), dtype=torch.bfloat16)
+    lse_like = torch.empty((w.T, w.H), dtype=torch.float32)
+    res_offs, res_total = packed([out_like, lse_like])
+    d_res = torch.empty(res_total, dtype=torch.uint8, device=dev)
+    h_res = torch.empty(res_total, dtype=torch.uint8).pin_memory()
+    d_out, d_lse = view(d_res, res_offs[0], out_like), view(d_res, res_offs[1], lse_like)
+    h2d = in_total
+    d2h = res_total
 
     def e2e_step():
-        d_ql = h_ql.to(dev, non_blocking=True)
-        d_qr = h_qr.to(dev, non_blocking=True)
-        d_tk = h_tk.to(dev, non_blocking=True)
-        d_nl, d_nr, d_ns = (h_nl.to(dev, non_blocking=True), h_nr.to(dev, non_blocking=True),
-                            h_ns.to(dev, non_blocking=True))
+        d_in.copy_(h_in, non_blocking=True)
         nvmla.nvfp4_mla_pack(d_nl, d_nr, d_ns, cache)
-        o, l = nvmla.sparse_mla_decode(d_ql, d_qr, cache, bt, d_tk, w.sm_scale, q_seq_idx=qs, seq_lens=sl,
-                                       workspace=ws, impl=impl)
-        h_out.copy_(o, non_blocking=True)
-        h_lse.copy_(l, non_blocking=True)
+        nvmla.sparse_mla_decode(d_ql, d_qr, cache, bt, d_tk, w.sm_scale, out=d_out, lse=d_lse, q_seq_idx=qs,
+                                seq_lens=sl, workspace=ws, impl=impl)
+        h_res.copy_(d_res, non_blocking=True)
 
     for _ in range(3):
         e2e_step()
     torch.cuda.synchronize()
+    # the host copy of the result matches the device-resident path's
+    if not (torch.equal(view(h_res, res_offs[0], out_like), out.cpu()) and
+            torch.equal(view(h_res, res_offs[1], lse_like), lse.cpu())):
+        raise RuntimeError("end-to-end result differs from the device-resident decode")
     e2e_ms = []
     for k in range(K):
         flush.fill_(float(k))

@@ -135,14 +135,16 @@ enum Bar {
   kBarKFreeA = 1,    // QK batch A done -> ring slots 0-2 reusable (commit)
   kBarKFullB = 2,    // K chunks 6-8 in ring slots 0-2 (8 unpack warps)
   kBarQKDone = 3,    // QK done: S^T full, every ring slot reusable (commit)
-  kBarPVReady = 4,   // P^T written (8 softmax warps) and V written (8 unpack warps)
+  kBarPVReady = 4,   // P^T written and V copied out of the K ring (8 softmax warps)
   kBarPVDone = 5,    // PV done: V tile and P^T buffer reusable, O^T settled (commit)
   kBarDrain = 6,     // every MMA finished (commit)
   kBarRx = 7,        // combine: the S partial slices have landed (TMA)
   kBarQ = 8,         // the raw query block has landed (TMA)
   kBarLastPV = 9,    // 4: block j of the last tile's PV done (commit)
   kBarRxMl = 13,     // combine: the S (m, l) blocks have landed (TMA)
-  kNumBars = 14
+  kBarVCopyA = 14,   // ring slots 0-2 copied into the V tile (8 softmax warps)
+  kBarVCopyB = 15,   // the rest of the tile's latent chunks copied (8 softmax warps)
+  kNumBars = 16
 };
 constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
 constexpr int kSmemBytes = kOffMisc + 16;
@@ -334,6 +336,14 @@ __device__ __forceinline__ bool softmax_sync_or(bool v) {
   return r != 0;
 }
 
+// maximum over the warp (every lane gets it); not volatile, so that
+// independent reductions can be issued back to back
+__device__ __forceinline__ float warp_max(float v) {
+  float r;
+  asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -402,52 +412,9 @@ __device__ __forceinline__ int32_t ldg_nc_s32(const int32_t* p) {
   return v;
 }
 
-// latent chunk of one row (64 dims) from its 32 code bytes and the 4 scale
-// bytes of its groups: 16-byte unit u holds dims 8u..8u+7 (group u / 2)
-__device__ __forceinline__ void write_chunk(const uint32_t (&c)[8], uint32_t scw, uint8_t* chunk, int r) {
-#pragma unroll
-  for (int g = 0; g < 4; ++g) {
-    const uint32_t s2 = e4m3_to_f16x2_bcast((scw >> (8 * g)) & 0xffu);
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      uint32_t h[4];
-      e2m1x8_to_f16x8(c[2 * g + q], h);
-      *reinterpret_cast<uint4*>(chunk + swz(r, 2 * g + q)) =
-          make_uint4(hmul2_u32(h[0], s2), hmul2_u32(h[1], s2), hmul2_u32(h[2], s2), hmul2_u32(h[3], s2));
-    }
-  }
-}
-
-// RoPE values 32h .. 32h + 31 of one row (units 4h .. 4h + 3 of the chunk)
-__device__ __forceinline__ void write_rope(const uint32_t (&v)[8], int h, uint8_t* chunk, int r) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint4 a;
-    e4m3x4_to_f16x4(v[2 * q], a.x, a.y);
-    e4m3x4_to_f16x4(v[2 * q + 1], a.z, a.w);
-    *reinterpret_cast<uint4*>(chunk + swz(r, 4 * h + q)) = a;
-  }
-}
-
-// E2M1 -> fp16 as in e2m1x8_to_f16x8, for the K copy of a chunk. The
-// unused operand `salt` makes this a different expression from the V copy's
-// conversion, so that the compiler converts each copy at its own time
-// instead of keeping 128 converted registers alive between the two.
-__device__ __forceinline__ void e2m1x8_to_f16x8_k(uint32_t w, uint32_t salt, uint32_t (&h)[4]) {
-  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
-      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
-      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
-      : "r"(w), "r"(salt));
-}
-
 // one row of a K chunk (64 dims = 32 columns of fp16 pairs) into this
 // thread's TMEM lane: column 4u + e holds dims 8u + 2e, 8u + 2e + 1
-__device__ __forceinline__ void tmem_store_chunk(const uint32_t (&c)[8], uint32_t scw, bool valid, uint32_t taddr,
-                                                 uint32_t salt) {
+__device__ __forceinline__ void tmem_store_chunk(const uint32_t (&c)[8], uint32_t scw, bool valid, uint32_t taddr) {
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
     uint32_t w[16];
@@ -458,7 +425,7 @@ __device__ __forceinline__ void tmem_store_chunk(const uint32_t (&c)[8], uint32_
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
         uint32_t h[4];
-        e2m1x8_to_f16x8_k(c[2 * g + q], salt, h);
+        e2m1x8_to_f16x8(c[2 * g + q], h);
 #pragma unroll
         for (int e = 0; e < 4; ++e) w[8 * g2 + 4 * q + e] = valid ? hmul2_u32(h[e], s2) : 0u;
       }
@@ -492,12 +459,6 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b), "r"(idesc), "r"(accum)
       : "memory");
-}
-
-__device__ __forceinline__ void zero_units(uint8_t* chunk, int r, int u0, int n) {
-#pragma unroll
-  for (int u = 0; u < 8; ++u)
-    if (u >= u0 && u < u0 + n) *reinterpret_cast<uint4*>(chunk + swz(r, u)) = make_uint4(0, 0, 0, 0);
 }
 
 // transposing butterfly: 32 values per lane -> lane L holds the reduction
@@ -661,7 +622,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
     mbar_init(bar(kBarKFreeA), 1);
     mbar_init(bar(kBarKFullB), 8);
     mbar_init(bar(kBarQKDone), 1);
-    mbar_init(bar(kBarPVReady), 16);
+    mbar_init(bar(kBarPVReady), 8);
+    mbar_init(bar(kBarVCopyA), 8);
+    mbar_init(bar(kBarVCopyB), 8);
     mbar_init(bar(kBarPVDone), 1);
     mbar_init(bar(kBarDrain), 1);
     mbar_init(bar(kBarRx), 1);
@@ -722,44 +685,37 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
       const bool valid = cur_slot >= 0;
       const int32_t nxt_slot = (i + 1 < ntiles) ? slots[(i + 1) * kTile + ur] : -1;
       const uint32_t sc[4] = {rs.x, rs.y, rs.z, rs.w};
-      // K batch A: latent chunks 4uh + 0..2 -> slots uh, 2 + uh, 4 + uh
-      if (i >= 1) ok = wait_bar_warp(bar(kBarQKDone), (i - 1) & 1, abort_flag, p.err_word);
+      // K batch A: latent chunks 4uh + 0..2 -> slots uh, 2 + uh, 4 + uh, once
+      // QK of the previous tile is done and its V has been copied out
+      if (i >= 1) {
+        ok = wait_bar_warp(bar(kBarQKDone), (i - 1) & 1, abort_flag, p.err_word);
+        if (ok) ok = wait_bar_warp(bar(kBarVCopyB), (i - 1) & 1, abort_flag, p.err_word);
+      }
       if (!ok) break;
       tc_fence_after();
 #pragma unroll
-      for (int j = 0; j < 3; ++j) tmem_store_chunk(rc[j], sc[j], valid, krow + 32 * (2 * j + uh), i);
+      for (int j = 0; j < 3; ++j) tmem_store_chunk(rc[j], sc[j], valid, krow + 32 * (2 * j + uh));
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc_fence_before();
       warp_arrive(bar(kBarKFullA), lane);
       if (tid == 0 && i < 2) NVMLA_TRACE_POINT(10 + 4 * i);
-      // K batch B: latent chunk 4uh + 3 -> slot uh; the RoPE chunk (half 0) -> slot 2;
-      // the RoPE bytes are requested now, their latency hidden by the wait
+      // K batch B: latent chunk 4uh + 3 -> slot uh; the RoPE chunk (half 0)
+      // -> slot 2; once batch A's MMAs are done and slots 0-2 copied to V.
+      // The RoPE bytes are requested first, their latency hidden by the waits.
       load_rope(cur_slot);
       ok = wait_bar_warp(bar(kBarKFreeA), i & 1, abort_flag, p.err_word);
+      if (ok) ok = wait_bar_warp(bar(kBarVCopyA), i & 1, abort_flag, p.err_word);
       if (!ok) break;
       tc_fence_after();
-      tmem_store_chunk(rc[3], sc[3], valid, krow + 32 * uh, i);
+      tmem_store_chunk(rc[3], sc[3], valid, krow + 32 * uh);
       if (uh == 0) tmem_store_rope(rr, valid, krow + 64);
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc_fence_before();
       warp_arrive(bar(kBarKFullB), lane);
       if (tid == 0 && i < 2) NVMLA_TRACE_POINT(11 + 4 * i);
-      // V (latent chunks 4uh + j) once PV of the previous tile has released
-      // the buffer; then these registers take the next tile's row
-      if (i >= 1) ok = wait_bar_warp(bar(kBarPVDone), (i - 1) & 1, abort_flag, p.err_word);
-      if (!ok) break;
+      // these registers now take the next tile's row
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint8_t* chunk = smem + kOffL + (4 * uh + j) * kChunkBytes;
-        if (valid) {
-          write_chunk(rc[j], sc[j], chunk, ur);
-        } else {
-          zero_units(chunk, ur, 0, 8);
-        }
-        load_codes(nxt_slot, j);
-      }
-      fence_async_smem();
-      warp_arrive(bar(kBarPVReady), lane);
+      for (int j = 0; j < 4; ++j) load_codes(nxt_slot, j);
       load_scale(nxt_slot);
       cur_slot = nxt_slot;
       if (tid == 0 && i < 2) NVMLA_TRACE_POINT(12 + 4 * i);
@@ -853,7 +809,54 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
     // S^T is free for the first tile
     warp_arrive(bar(kBarKFullA), lane);
     ok = !softmax_sync_or(*abort_flag != 0);
+    // V tile i from the K ring (its latent chunks are the V operand's rows):
+    // this warp copies columns 16hh..16hh+15 of each ring slot, row k
+    uint8_t* vrow = smem + kOffL;
+    auto copy_slot = [&](int slot, int chunk) {
+      uint8_t* dst = vrow + chunk * kChunkBytes;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t w[8];
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+                     : "r"(tmem + lane_base + kColK + 32 * slot + 16 * hh + 8 * half));
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+          *reinterpret_cast<uint4*>(dst + swz(quad * 32 + lane, 4 * hh + 2 * half + q)) =
+              make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+      }
+    };
     for (int i = 0; i < ntiles && ok; ++i) {
+      // part A: slots 0-2 hold latent chunks 0, 4, 1 until batch B reuses
+      // them; the V tile is free once PV of the previous tile is done
+      ok = wait_bar_warp(bar(kBarKFullA), i & 1, abort_flag, p.err_word);
+      if (ok && i >= 1) ok = wait_bar_warp(bar(kBarPVDone), (i - 1) & 1, abort_flag, p.err_word);
+      if (softmax_sync_or(!ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      copy_slot(0, 0);
+      copy_slot(1, 4);
+      copy_slot(2, 1);
+      tc_fence_before();
+      warp_arrive(bar(kBarVCopyA), lane);
+      // part B: chunks 3, 7 (slots 0, 1, batch B) and 5, 2, 6 (slots 3-5)
+      ok = wait_bar_warp(bar(kBarKFullB), i & 1, abort_flag, p.err_word);
+      if (softmax_sync_or(!ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      copy_slot(0, 3);
+      copy_slot(1, 7);
+      copy_slot(3, 5);
+      copy_slot(4, 2);
+      copy_slot(5, 6);
+      fence_async_smem();
+      tc_fence_before();
+      warp_arrive(bar(kBarVCopyB), lane);
       ok = wait_bar_warp(bar(kBarQKDone), i & 1, abort_flag, p.err_word);
       if (softmax_sync_or(!ok)) {
         ok = false;
@@ -877,16 +880,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
         }
       }
       const bool slow = softmax_sync_or(excess > kTau);
-      bool pv_done = i == 0;  // PV of the previous tile has finished
-      if (!slow) {
-        // S^T is in registers: QK of the next tile may overwrite it
-        tc_fence_before();
-        warp_arrive(bar(kBarKFullA), lane);
-      } else {
-        // exact per-head maximum of this tile (destroys s, reloaded below
-        // before S^T is released)
-        warp_reduce32<true>(s, lane);
-        red[quad * 64 + hb + lane] = s[0];
+      // (PV of the previous tile has finished: waited for before the V copy)
+      // S^T is in registers: QK of the next tile may overwrite it
+      tc_fence_before();
+      warp_arrive(bar(kBarKFullA), lane);
+      if (slow) {
+        // exact per-head maximum of this tile: warp reductions that leave s
+        // intact, then across the four lane quadrants
+        float mine = -INFINITY;
+#pragma unroll
+        for (int h = 0; h < 32; ++h) {
+          const float mh = warp_max(s[h]);
+          mine = lane == h ? mh : mine;
+        }
+        red[quad * 64 + hb + lane] = mine;
         softmax_sync();
         if (quad == 0) {
           const int h = hb + lane;
@@ -905,15 +912,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
           lp[4 * h4 + 2] *= a4.z;
           lp[4 * h4 + 3] *= a4.w;
         }
-        tmem_ld32f(tmem + lane_base + kColS + hb, s);
-#pragma unroll
-        for (int h = 0; h < 32; ++h) s[h] = valid ? s[h] * p.sl2 : -INFINITY;
-        tc_fence_before();
-        warp_arrive(bar(kBarKFullA), lane);
         if (i >= 1) {
-          // O^T must hold the finished PV of every earlier tile
-          ok = wait_bar_warp(bar(kBarPVDone), (i - 1) & 1, abort_flag, p.err_word);
-          pv_done = true;
+          // O^T holds the finished PV of every earlier tile
           tc_fence_after();
           if (ok) {
             // 16 columns at a time
@@ -947,7 +947,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
       }
       // P^T row (this thread's 32 heads) -> R, once PV of the previous tile
       // has read it
-      if (!pv_done) ok = wait_bar_warp(bar(kBarPVDone), (i - 1) & 1, abort_flag, p.err_word);
       uint8_t* pt = smem + kOffR;
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
