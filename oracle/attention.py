@@ -13,7 +13,9 @@ definition exactly in float64.
 Definition, per query token t and head h (readings listed in the design
 notes):
 
-* b = q_seq_idx[t] (0 if absent); the valid set J(t) holds every slot k whose
+* b = q_seq_idx[t] (0 if absent). A token whose b lies outside the block
+  table's rows has no valid slot: every entry other than -1 is a bad index.
+* the valid set J(t) holds every slot k whose
   position p = topk_idx[t, k] satisfies 0 <= p < seq_lens[b] (and p inside the
   block table). A slot equal to -1 is padding. Any other out-of-range value
   is also skipped and counted as a bad index. Duplicated positions count
@@ -53,6 +55,8 @@ def select_rows(topk_row, seq, block_table, seq_len, num_slots):
     Returns (slots [n] int64, n_bad) where n_bad counts entries that are
     neither -1 nor a valid position."""
     p = np.asarray(topk_row, dtype=np.int64)
+    if not 0 <= seq < block_table.shape[0]:
+        return np.zeros(0, dtype=np.int64), int((p != -1).sum())
     max_pos = block_table.shape[1] * PAGE_TOKENS
     limit = max_pos if seq_len is None else min(int(seq_len), max_pos)
     valid = (p >= 0) & (p < limit)
@@ -100,7 +104,7 @@ def sparse_mla_decode(q_latent, q_rope, cache, block_table, topk_idx, sm_scale,
     outs, lses, n_bad = [], [], 0
     for t in toks:
         b = 0 if qs is None else int(qs[t])
-        L = None if sl is None else int(sl[b])
+        L = None if sl is None or not 0 <= b < bt.shape[0] else int(sl[b])
         slots, bad = select_rows(topk[t], b, bt, L, cache.shape[0])
         n_bad += bad
         K_lat, K_rope = _pack.unpack_rows(cache[slots])

@@ -11,6 +11,7 @@ import pytest
 import torch
 
 import parity
+from oracle import attention as oatt
 from nvfp4_sparse_mla_gb300 import workloads
 
 pytestmark = pytest.mark.gpu
@@ -152,6 +153,29 @@ def test_bad_indices_masked_and_counted(lib, cuda, impl):
     parity.assert_close(out, lse, ro, rl, "bad indices")
     e = err.cpu().tolist()
     assert e[0] & 0x1 and e[1] == 3
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_bad_sequence_index_masks_the_token(lib, cuda, impl):
+    """A query token whose sequence index has no block-table row reads
+    nothing (out 0, lse -inf) and every entry of its list other than -1 is
+    counted; the other tokens of the call are unaffected."""
+    w = workloads.padded(seed=10, T=3, H=64, ctx=1200, topk=160, max_pad_frac=0.2)
+    cache = parity.device_cache(lib, w, cuda)
+    ref_cache = parity.oracle_cache(w)
+    qs = w.q_seq_idx.clone()
+    qs[1] = 5  # the workload has one sequence
+    err = torch.zeros(2, dtype=torch.int32, device=cuda)
+    d = parity.device_inputs(w, cuda)
+    out, lse = lib.sparse_mla_decode(d["q_latent"], d["q_rope"], cache, d["block_table"], d["topk_idx"], w.sm_scale,
+                                     q_seq_idx=qs.to(cuda), seq_lens=d["seq_lens"], err_word=err,
+                                     impl=_impl(lib, impl))
+    ro, rl, bad = oatt.sparse_mla_decode(w.q_latent, w.q_rope, ref_cache, w.block_table, w.topk_idx, w.sm_scale,
+                                         qs, w.seq_lens)
+    assert bad == int((w.topk_idx[1] != -1).sum())
+    parity.assert_close(out, lse, ro, rl, "bad sequence index")
+    e = err.cpu().tolist()
+    assert e[0] & 0x1 and e[1] == bad
 
 
 @pytest.mark.parametrize("impl", IMPLS)

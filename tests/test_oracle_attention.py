@@ -264,3 +264,24 @@ def test_staged_requantisation_matches_torch_float8():
             ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
             assert np.array_equal(buf[t, k, :512], ref)
             assert np.array_equal(buf[t, k, 512:], p["logical"][b][pos][288:352])
+
+
+def test_sequence_index_outside_the_table_selects_nothing():
+    """A token whose sequence index has no block-table row attends to
+    nothing (out 0, lse -inf); each of its entries other than -1 counts as a
+    bad index. Checked against a token of a valid sequence in the same call."""
+    rng = np.random.default_rng(21)
+    bt = np.arange(4, dtype=np.int64).reshape(1, 4)
+    cache = rng.integers(0, 256, size=(4, 64, 352), dtype=np.uint8)
+    cache[:, :, 256:288] = 0x30  # finite scales
+    cache[:, :, 288:] = 0x38     # finite RoPE
+    ql = rng.standard_normal((2, 16, 512))
+    qr = rng.standard_normal((2, 16, 64))
+    topk = np.array([[3, 17, -1, 200], [3, 17, -1, 200]], dtype=np.int64)
+    out, lse, bad = attention.sparse_mla_decode(ql, qr, cache, bt, topk, 0.1, q_seq_idx=np.array([0, 2]),
+                                           seq_lens=np.array([256]))
+    assert bad == 3
+    assert np.all(out[1] == 0) and np.all(np.isneginf(lse[1]))
+    assert np.all(np.isfinite(lse[0]))
+    ref_out, ref_lse, _ = attention.sparse_mla_decode(ql[:1], qr[:1], cache, bt, topk[:1], 0.1, seq_lens=np.array([256]))
+    assert np.array_equal(out[0], ref_out[0]) and np.array_equal(lse[0], ref_lse[0])
