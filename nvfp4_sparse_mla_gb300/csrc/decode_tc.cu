@@ -99,8 +99,9 @@ constexpr int kHeads = 64;              // heads per CTA (MMA N)
 constexpr int kMaxTiles = 16;           // 2048 slots
 constexpr int kUnpackThreads = 256;     // warps 0-7
 constexpr int kSoftmax0 = 256;          // warps 8-15: threads 256..511
-constexpr int kMmaWarp = 16;            // issues every MMA; allocates TMEM
-constexpr int kThreads = 544;           // 17 warps
+constexpr int kQkWarp = 16;             // issues the QK MMAs; allocates TMEM
+constexpr int kPvWarp = 17;             // issues the PV MMAs
+constexpr int kThreads = 576;           // 18 warps
 constexpr int kMaxCluster = 16;         // CTAs sharing one token
 constexpr int kChunkBytes = 16384;      // 128 rows x 128 bytes
 constexpr uint32_t kTmemCols = 512;
@@ -626,7 +627,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
     mbar_init(bar(kBarVCopyA), 8);
     mbar_init(bar(kBarVCopyB), 8);
     mbar_init(bar(kBarPVDone), 1);
-    mbar_init(bar(kBarDrain), 1);
+    mbar_init(bar(kBarDrain), 2);
     mbar_init(bar(kBarRx), 1);
     mbar_init(bar(kBarRxMl), 1);
     for (int j = 0; j < 4; ++j) mbar_init(bar(kBarLastPV + j), 1);
@@ -634,7 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (tid < kHeads) m_run[tid] = -INFINITY;
-  if (warp == kMmaWarp) {
+  if (warp == kQkWarp) {
     __syncwarp();
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                  "r"(kTmemCols)
@@ -720,87 +721,90 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
       cur_slot = nxt_slot;
       if (tid == 0 && i < 2) NVMLA_TRACE_POINT(12 + 4 * i);
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == kQkWarp || warp == kPvWarp) {
     // ------------------------------------------------------------ MMA issue
-    // Per tile: QK batch A (24 MMAs), PV of the previous tile (32), QK batch
-    // B (12); one wait before each batch, one commit after it. The softmax
-    // of a tile thus overlaps QK of the next.
+    // Two issuing threads on different SM sub-partitions: one issues QK
+    // (batch A, 24 MMAs, and batch B, 12, per tile), the other PV (32 per
+    // tile). A thread issuing tcgen05.mma competes for issue with the other
+    // warps of its sub-partition, so one issuer alone cannot keep the tensor
+    // core busy; the two streams touch different accumulators and are
+    // ordered only through the barriers. One wait before each batch, one
+    // commit after it, straight-line loops in between.
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_f16(false, false);
       constexpr uint32_t idesc_pv = idesc_f16(true, true);
       const uint32_t lb = sbase + kOffL, rb = sbase + kOffR, qb = sbase + kOffQ;
       const uint32_t ring = tmem + kColK;
       bool mok = *abort_flag == 0;
-      // (the last tile's PV also reports each block, so that the epilogue
-      // can start on it; two straight-line copies, as a conditional branch
-      // between MMAs costs the issue)
-      auto issue_pv = [&](int i) {
+      if (warp == kPvWarp) {
+        // (the last tile's PV also reports each block, so that the epilogue
+        // can start on it; a separate copy, as a conditional branch between
+        // MMAs costs the issue)
+        auto issue_pv = [&](int i) {
 #pragma unroll 1
-        for (int j = 0; j < 4; ++j) {
+          for (int j = 0; j < 4; ++j) {
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            mma_f16(tmem + kColO + 64 * j, sdesc(lb + j * kChunkBytes + 2048 * ks, 4 * kChunkBytes, 1024),
-                    sdesc(rb + 2048 * ks, 8192, 1024), idesc_pv, (i | ks) != 0);
-        }
-        mma_commit(bar(kBarPVDone));
-      };
-      auto issue_pv_last = [&](int i) {
+            for (int ks = 0; ks < 8; ++ks)
+              mma_f16(tmem + kColO + 64 * j, sdesc(lb + j * kChunkBytes + 2048 * ks, 4 * kChunkBytes, 1024),
+                      sdesc(rb + 2048 * ks, 8192, 1024), idesc_pv, (i | ks) != 0);
+          }
+          mma_commit(bar(kBarPVDone));
+        };
+        auto issue_pv_last = [&](int i) {
 #pragma unroll 1
-        for (int j = 0; j < 4; ++j) {
+          for (int j = 0; j < 4; ++j) {
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            mma_f16(tmem + kColO + 64 * j, sdesc(lb + j * kChunkBytes + 2048 * ks, 4 * kChunkBytes, 1024),
-                    sdesc(rb + 2048 * ks, 8192, 1024), idesc_pv, (i | ks) != 0);
-          mma_commit(bar(kBarLastPV + j));
-        }
-        mma_commit(bar(kBarPVDone));
-      };
-      for (int i = 0; i < ntiles && mok; ++i) {
-        mok = wait_bar(bar(kBarKFullA), i & 1, abort_flag, p.err_word);
-        if (!mok) break;
-        tc_fence_after();
-        // batch A: uses 0..5 (slot u, query chunk 4 (u & 1) + u / 2); loop
-        // back-edges, unlike conditional branches, cost the issue nothing
-#pragma unroll 1
-        for (int u = 0; u < 6; ++u) {
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            mma_f16_ts(tmem + kColS, ring + 32 * u + 8 * ks,
-                       sdesc(qb + (4 * (u & 1) + (u >> 1)) * 8192 + 32 * ks, 16, 1024), idesc_qk, (u | ks) != 0);
-        }
-        mma_commit(bar(kBarKFreeA));
-        if (i >= 1) {
-          mok = wait_bar(bar(kBarPVReady), (i - 1) & 1, abort_flag, p.err_word);
+            for (int ks = 0; ks < 8; ++ks)
+              mma_f16(tmem + kColO + 64 * j, sdesc(lb + j * kChunkBytes + 2048 * ks, 4 * kChunkBytes, 1024),
+                      sdesc(rb + 2048 * ks, 8192, 1024), idesc_pv, (i | ks) != 0);
+            mma_commit(bar(kBarLastPV + j));
+          }
+          mma_commit(bar(kBarPVDone));
+        };
+        for (int i = 0; i < ntiles && mok; ++i) {
+          mok = wait_bar(bar(kBarPVReady), i & 1, abort_flag, p.err_word);
           if (!mok) break;
           tc_fence_after();
-          issue_pv(i - 1);
+          if (i + 1 < ntiles) {
+            issue_pv(i);
+          } else {
+            issue_pv_last(i);
+          }
         }
-        mok = wait_bar(bar(kBarKFullB), i & 1, abort_flag, p.err_word);
-        if (!mok) break;
-        tc_fence_after();
-        // batch B: uses 6, 7 (latent chunks 3, 7) in slots 0, 1; use 8 (RoPE) in slot 2
-#pragma unroll 1
-        for (int u = 0; u < 3; ++u) {
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            mma_f16_ts(tmem + kColS, ring + 32 * u + 8 * ks, sdesc(qb + (u == 2 ? 8 : 3 + 4 * u) * 8192 + 32 * ks, 16, 1024),
-                       idesc_qk, 1);
-        }
-        mma_commit(bar(kBarQKDone));
-      }
-      if (mok && ntiles > 0) {
-        mok = wait_bar(bar(kBarPVReady), (ntiles - 1) & 1, abort_flag, p.err_word);
-        if (mok) {
+      } else {
+        for (int i = 0; i < ntiles && mok; ++i) {
+          mok = wait_bar(bar(kBarKFullA), i & 1, abort_flag, p.err_word);
+          if (!mok) break;
           tc_fence_after();
-          issue_pv_last(ntiles - 1);
+          // batch A: uses 0..5 (slot u, query chunk 4 (u & 1) + u / 2)
+#pragma unroll 1
+          for (int u = 0; u < 6; ++u) {
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              mma_f16_ts(tmem + kColS, ring + 32 * u + 8 * ks,
+                         sdesc(qb + (4 * (u & 1) + (u >> 1)) * 8192 + 32 * ks, 16, 1024), idesc_qk, (u | ks) != 0);
+          }
+          mma_commit(bar(kBarKFreeA));
+          mok = wait_bar(bar(kBarKFullB), i & 1, abort_flag, p.err_word);
+          if (!mok) break;
+          tc_fence_after();
+          // batch B: uses 6, 7 (latent chunks 3, 7) in slots 0, 1; use 8 (RoPE) in slot 2
+#pragma unroll 1
+          for (int u = 0; u < 3; ++u) {
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              mma_f16_ts(tmem + kColS, ring + 32 * u + 8 * ks,
+                         sdesc(qb + (u == 2 ? 8 : 3 + 4 * u) * 8192 + 32 * ks, 16, 1024), idesc_qk, 1);
+          }
+          mma_commit(bar(kBarQKDone));
         }
       }
-      // every MMA issued has finished once this commit lands
+      // every MMA this thread issued has finished once both issuers' commits land
       mma_commit(bar(kBarDrain));
       wait_bar_drain(bar(kBarDrain), 0);
     }
     __syncwarp();
-  } else {
+  } else if (is_softmax) {
     // ------------------------------------------------------------ softmax
     const int k = quad * 32 + lane;  // row of this thread
     float lp[32];  // this row's share of its heads' sums
@@ -1040,7 +1044,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
 
   // ------------------------------------------------------------ combine
   __syncthreads();  // every role is done with TMEM
-  if (warp == kMmaWarp) {
+  if (warp == kQkWarp) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
   }
