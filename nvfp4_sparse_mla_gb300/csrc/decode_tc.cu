@@ -111,7 +111,7 @@ constexpr uint32_t kColK = 320;         // K ring: kRing slots of 32 columns (64
 constexpr int kRing = 6;                // a tile's 9 K chunks: batch A = chunk uses 0-5 in slots 0-5,
                                         // batch B = uses 6-8 in slots 0-2
 static_assert(kColK + 32 * kRing <= kTmemCols, "TMEM budget");
-constexpr float kTau = 8.0f;            // rescale threshold, log2 units
+constexpr float kTau = 15.0f;           // rescale threshold, log2 units: P < 2^15 fits fp16
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr int kPartBytes = kLatent * kHeads * 2;  // one CTA's fp16 partial: 64 KB
 constexpr int kMlBytes = kHeads * 8;              // its per-head (m, l)
@@ -693,6 +693,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
         if (ok) ok = wait_bar_warp(bar(kBarVCopyB), (i - 1) & 1, abort_flag, p.err_word);
       }
       if (!ok) break;
+      if (tid == 0 && i < 2) NVMLA_TRACE_POINT(70 + 10 * i);
       tc_fence_after();
 #pragma unroll
       for (int j = 0; j < 3; ++j) tmem_store_chunk(rc[j], sc[j], valid, krow + 32 * (2 * j + uh));
@@ -707,6 +708,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
       ok = wait_bar_warp(bar(kBarKFreeA), i & 1, abort_flag, p.err_word);
       if (ok) ok = wait_bar_warp(bar(kBarVCopyA), i & 1, abort_flag, p.err_word);
       if (!ok) break;
+      if (tid == 0 && i < 2) NVMLA_TRACE_POINT(72 + 10 * i);
       tc_fence_after();
       tmem_store_chunk(rc[3], sc[3], valid, krow + 32 * uh);
       if (uh == 0) tmem_store_rope(rr, valid, krow + 64);
@@ -765,17 +767,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
           mok = wait_bar(bar(kBarPVReady), i & 1, abort_flag, p.err_word);
           if (!mok) break;
           tc_fence_after();
+          if (i < 2) NVMLA_TRACE_POINT(60 + 6 * i);
           if (i + 1 < ntiles) {
             issue_pv(i);
           } else {
             issue_pv_last(i);
           }
+          if (i < 2) NVMLA_TRACE_POINT(61 + 6 * i);
         }
       } else {
         for (int i = 0; i < ntiles && mok; ++i) {
           mok = wait_bar(bar(kBarKFullA), i & 1, abort_flag, p.err_word);
           if (!mok) break;
           tc_fence_after();
+          if (i < 2) NVMLA_TRACE_POINT(50 + 8 * i);
           // batch A: uses 0..5 (slot u, query chunk 4 (u & 1) + u / 2)
 #pragma unroll 1
           for (int u = 0; u < 6; ++u) {
@@ -785,9 +790,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
                          sdesc(qb + (4 * (u & 1) + (u >> 1)) * 8192 + 32 * ks, 16, 1024), idesc_qk, (u | ks) != 0);
           }
           mma_commit(bar(kBarKFreeA));
+          if (i < 2) NVMLA_TRACE_POINT(51 + 8 * i);
           mok = wait_bar(bar(kBarKFullB), i & 1, abort_flag, p.err_word);
           if (!mok) break;
           tc_fence_after();
+          if (i < 2) NVMLA_TRACE_POINT(54 + 8 * i);
           // batch B: uses 6, 7 (latent chunks 3, 7) in slots 0, 1; use 8 (RoPE) in slot 2
 #pragma unroll 1
           for (int u = 0; u < 3; ++u) {
@@ -797,6 +804,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
                          sdesc(qb + (u == 2 ? 8 : 3 + 4 * u) * 8192 + 32 * ks, 16, 1024), idesc_qk, 1);
           }
           mma_commit(bar(kBarQKDone));
+          if (i < 2) NVMLA_TRACE_POINT(55 + 8 * i);
         }
       }
       // every MMA this thread issued has finished once both issuers' commits land
@@ -846,7 +854,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
       copy_slot(2, 1);
       tc_fence_before();
       warp_arrive(bar(kBarVCopyA), lane);
-      // part B: chunks 3, 7 (slots 0, 1, batch B) and 5, 2, 6 (slots 3-5)
+      if (tid == kSoftmax0 && i < 2) NVMLA_TRACE_POINT(104 + 10 * i);
+      // chunks 5, 2, 6 (slots 3-5, which batch B leaves alone) while the
+      // unpack fills batch B
+      copy_slot(3, 5);
+      copy_slot(4, 2);
+      copy_slot(5, 6);
+      // part B: chunks 3, 7 (slots 0, 1, batch B)
       ok = wait_bar_warp(bar(kBarKFullB), i & 1, abort_flag, p.err_word);
       if (softmax_sync_or(!ok)) {
         ok = false;
@@ -855,12 +869,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
       tc_fence_after();
       copy_slot(0, 3);
       copy_slot(1, 7);
-      copy_slot(3, 5);
-      copy_slot(4, 2);
-      copy_slot(5, 6);
       fence_async_smem();
       tc_fence_before();
       warp_arrive(bar(kBarVCopyB), lane);
+      if (tid == kSoftmax0 && i < 2) NVMLA_TRACE_POINT(105 + 10 * i);
       ok = wait_bar_warp(bar(kBarQKDone), i & 1, abort_flag, p.err_word);
       if (softmax_sync_or(!ok)) {
         ok = false;
@@ -871,8 +883,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
       const bool valid = slots[i * kTile + k] >= 0;
       float s[32];
       tmem_ld32f(tmem + lane_base + kColS + hb, s);
+      if (tid == kSoftmax0 && i < 2) NVMLA_TRACE_POINT(100 + 10 * i);
 #pragma unroll
       for (int h = 0; h < 32; ++h) s[h] = valid ? s[h] * p.sl2 : -INFINITY;
+      if (i == 0) {
+        // the running maximum starts at row 0's scores (-inf if that row is
+        // masked): any value that some score reaches is a valid reference,
+        // and the exact reduction below runs only if a score of the tile
+        // lies more than 2^tau above it
+        if (k == 0) {
+#pragma unroll
+          for (int h4 = 0; h4 < 8; ++h4)
+            *reinterpret_cast<float4*>(m_run + hb + 4 * h4) =
+                make_float4(s[4 * h4], s[4 * h4 + 1], s[4 * h4 + 2], s[4 * h4 + 3]);
+        }
+        softmax_sync();
+      }
       // does any score exceed its head's running maximum by more than 2^tau?
       float excess = -INFINITY;
       if (valid) {
@@ -884,6 +910,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
         }
       }
       const bool slow = softmax_sync_or(excess > kTau);
+      if (tid == kSoftmax0 && i < 2) NVMLA_TRACE_POINT(101 + 10 * i);
       // (PV of the previous tile has finished: waited for before the V copy)
       // S^T is in registers: QK of the next tile may overwrite it
       tc_fence_before();
@@ -949,6 +976,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
           lp[h] += pv;
         }
       }
+      if (tid == kSoftmax0 && i < 2) NVMLA_TRACE_POINT(102 + 10 * i);
       // P^T row (this thread's 32 heads) -> R, once PV of the previous tile
       // has read it
       uint8_t* pt = smem + kOffR;
