@@ -88,9 +88,22 @@ __device__ unsigned long long nvmla_tc_trace[kTraceCtas][kTracePoints];
       nvmla_tc_trace[cta_][(id)] = t_;                                                               \
     }                                                                                                \
   } while (0)
+// the same, once the 32-bit value v is available
+#define NVMLA_TRACE_AFTER(id, v)                                                                     \
+  do {                                                                                               \
+    const int cta_ = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);                  \
+    if (cta_ < kTraceCtas) {                                                                         \
+      unsigned long long t_;                                                                         \
+      asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t_) : "r"(v));                                \
+      nvmla_tc_trace[cta_][(id)] = t_;                                                               \
+    }                                                                                                \
+  } while (0)
 #else
 #define NVMLA_TRACE_POINT(id) \
   do {                        \
+  } while (0)
+#define NVMLA_TRACE_AFTER(id, v) \
+  do {                           \
   } while (0)
 #endif
 
@@ -565,10 +578,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
     }
     return static_cast<int32_t>(s);
   };
+  // the physical row of pos, if it has one, before the sequence length is
+  // known: its bytes are requested early and ignored when the row turns out
+  // to lie past the sequence's end
+  auto phys_slot = [&](int32_t pos, int32_t page) -> int32_t {
+    if (!seq_ok || pos < 0 || (pos >> 6) >= p.sel.max_pages || page < 0) return -1;
+    const int64_t s = static_cast<int64_t>(page) * kPage + (pos & 63);
+    return s < p.sel.num_slots ? static_cast<int32_t>(s) : -1;
+  };
   int32_t page0 = 0;
   int32_t pagel[kLaterPer];
+  if (tid == 0) NVMLA_TRACE_AFTER(3, pos0);
+  if (tid == 0) NVMLA_TRACE_AFTER(4, seq_raw);
   if (is_unpack) {
     page0 = page_of(pos0);
+    if (tid == 0) NVMLA_TRACE_AFTER(5, page0);
   } else if (is_softmax) {
 #pragma unroll
     for (int m = 0; m < kLaterPer; ++m) pagel[m] = (1 + (sj >> 7) + 2 * m < ntiles) ? page_of(posl[m]) : 0;
@@ -579,8 +603,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
     limit = L < limit ? L : limit;
   }
 
-  // ---- level 3: rows of the first tile (unpack threads, into registers),
-  // L2 prefetch of the later tiles' rows (softmax threads)
+  // ---- level 3: rows of the first tile (unpack threads, into registers);
+  // the later tiles' slots (softmax threads)
   uint32_t rc[4][8];  // code bytes of latent chunks 4uh + j
   uint4 rs;           // scale bytes of groups 16uh .. 16uh + 15
   uint32_t rr[16];    // the 64 RoPE bytes (half 0 only)
@@ -599,20 +623,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
     }
   };
   if (is_unpack) {
-    if (ntiles > 0 && kbeg + ur < kend) slot0 = classify(pos0, page0, limit, report && uh == 0);
+    const bool mine = ntiles > 0 && kbeg + ur < kend;
+    const int32_t sspec = mine ? phys_slot(pos0, page0) : -1;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) load_codes(slot0, j);
-    load_scale(slot0);
+    for (int j = 0; j < 4; ++j) load_codes(sspec, j);
+    load_scale(sspec);
+    if (mine) slot0 = classify(pos0, page0, limit, report && uh == 0);
     if (uh == 0) slots[ur] = slot0;
   } else if (is_softmax) {
 #pragma unroll
     for (int m = 0; m < kLaterPer; ++m) {
       const int i = 1 + (sj >> 7) + 2 * m;
-      if (i < ntiles) {
-        const int32_t s = classify(posl[m], pagel[m], limit, report);
-        slots[i * kTile + (sj & 127)] = s;
-        if (s >= 0) prefetch_l2(p.cache + static_cast<int64_t>(s) * kRowBytes, kRowBytes);
-      }
+      if (i < ntiles) slots[i * kTile + (sj & 127)] = classify(posl[m], pagel[m], limit, report);
     }
   }
   if (tid == 0) NVMLA_TRACE_POINT(1);
@@ -650,6 +672,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
   // query block -> fp16, K-major 128B-swizzled (4608 pieces of 16 bytes);
   // then the latent tile's space is free for the unpack
   if (wait_bar_warp(bar(kBarQ), 0, abort_flag, p.err_word)) {
+    if (tid == 0) NVMLA_TRACE_POINT(6);
     const uint8_t* qraw = smem + kOffL;
     for (int i = tid; i < kHeads * 72; i += kThreads) {
       const int h = i / 72, j = i % 72, c = j >> 3, q = j & 7;
@@ -662,6 +685,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
       *reinterpret_cast<uint4*>(smem + kOffQ + c * 8192 + swz(h, q)) = make_uint4(o[0], o[1], o[2], o[3]);
     }
   }
+  if (tid == 0) NVMLA_TRACE_POINT(7);
   fence_async_smem();
   __syncthreads();
   if (*abort_flag && tid == 0) report_error(p.err_word, NVMLA_ERRW_WAIT_TIMEOUT, 1);
@@ -682,6 +706,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
     ok = *abort_flag == 0;
     int32_t cur_slot = slot0;
     const uint32_t krow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + kColK;  // this row's lane
+    if (tid == 0) NVMLA_TRACE_AFTER(8, rc[0][0]);
     for (int i = 0; i < ntiles && ok; ++i) {
       const bool valid = cur_slot >= 0;
       const int32_t nxt_slot = (i + 1 < ntiles) ? slots[(i + 1) * kTile + ur] : -1;
@@ -818,6 +843,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
     float lp[32];  // this row's share of its heads' sums
 #pragma unroll
     for (int h = 0; h < 32; ++h) lp[h] = 0.f;
+    // the later tiles' rows to L2, now that the first tile's are in flight
+    // (requested together with them, they delay them)
+    for (int i = 1 + (sj >> 7); i < ntiles; i += 2) {
+      const int32_t sl = slots[i * kTile + (sj & 127)];
+      if (sl >= 0) prefetch_l2(p.cache + static_cast<int64_t>(sl) * kRowBytes, kRowBytes);
+    }
     // S^T is free for the first tile
     warp_arrive(bar(kBarKFullA), lane);
     ok = !softmax_sync_or(*abort_flag != 0);
