@@ -158,7 +158,8 @@ enum Bar {
   kBarRxMl = 13,     // combine: the S (m, l) blocks have landed (TMA)
   kBarVCopyA = 14,   // ring slots 0-2 copied into the V tile (8 softmax warps)
   kBarVCopyB = 15,   // the rest of the tile's latent chunks copied (8 softmax warps)
-  kNumBars = 16
+  kBarPVHalf = 16,   // PV blocks 0-1 done: V chunks 0, 1, 4, 5 reusable (commit)
+  kNumBars = 17
 };
 constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
 constexpr int kSmemBytes = kOffMisc + 16;
@@ -649,6 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
     mbar_init(bar(kBarVCopyA), 8);
     mbar_init(bar(kBarVCopyB), 8);
     mbar_init(bar(kBarPVDone), 1);
+    mbar_init(bar(kBarPVHalf), 1);
     mbar_init(bar(kBarDrain), 2);
     mbar_init(bar(kBarRx), 1);
     mbar_init(bar(kBarRxMl), 1);
@@ -767,9 +769,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
         // (the last tile's PV also reports each block, so that the epilogue
         // can start on it; a separate copy, as a conditional branch between
         // MMAs costs the issue)
+        // (block j reads V chunks j and j + 4; after blocks 0-1 the next
+        // tile's V copy may start on chunks 0, 1, 4, 5)
         auto issue_pv = [&](int i) {
 #pragma unroll 1
-          for (int j = 0; j < 4; ++j) {
+          for (int j = 0; j < 2; ++j) {
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+              mma_f16(tmem + kColO + 64 * j, sdesc(lb + j * kChunkBytes + 2048 * ks, 4 * kChunkBytes, 1024),
+                      sdesc(rb + 2048 * ks, 8192, 1024), idesc_pv, (i | ks) != 0);
+          }
+          mma_commit(bar(kBarPVHalf));
+#pragma unroll 1
+          for (int j = 2; j < 4; ++j) {
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)
               mma_f16(tmem + kColO + 64 * j, sdesc(lb + j * kChunkBytes + 2048 * ks, 4 * kChunkBytes, 1024),
@@ -872,9 +884,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
     };
     for (int i = 0; i < ntiles && ok; ++i) {
       // part A: slots 0-2 hold latent chunks 0, 4, 1 until batch B reuses
-      // them; the V tile is free once PV of the previous tile is done
+      // them; their V chunks are free once PV blocks 0-1 of the previous
+      // tile are done
       ok = wait_bar_warp(bar(kBarKFullA), i & 1, abort_flag, p.err_word);
-      if (ok && i >= 1) ok = wait_bar_warp(bar(kBarPVDone), (i - 1) & 1, abort_flag, p.err_word);
+      if (ok && i >= 1) ok = wait_bar_warp(bar(kBarPVHalf), (i - 1) & 1, abort_flag, p.err_word);
       if (softmax_sync_or(!ok)) {
         ok = false;
         break;
@@ -887,8 +900,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
       warp_arrive(bar(kBarVCopyA), lane);
       if (tid == kSoftmax0 && i < 2) NVMLA_TRACE_POINT(104 + 10 * i);
       // chunks 5, 2, 6 (slots 3-5, which batch B leaves alone) while the
-      // unpack fills batch B
+      // unpack fills batch B; chunks 2 and 6 once the whole PV is done
       copy_slot(3, 5);
+      if (i >= 1) ok = wait_bar_warp(bar(kBarPVDone), (i - 1) & 1, abort_flag, p.err_word);
+      if (softmax_sync_or(!ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
       copy_slot(4, 2);
       copy_slot(5, 6);
       // part B: chunks 3, 7 (slots 0, 1, batch B)
@@ -917,22 +936,34 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
       if (tid == kSoftmax0 && i < 2) NVMLA_TRACE_POINT(100 + 10 * i);
 #pragma unroll
       for (int h = 0; h < 32; ++h) s[h] = valid ? s[h] * p.sl2 : -INFINITY;
+      // does any score exceed its head's running maximum by more than 2^tau?
+      float excess = -INFINITY;
       if (i == 0) {
-        // the running maximum starts at row 0's scores (-inf if that row is
-        // masked): any value that some score reaches is a valid reference,
-        // and the exact reduction below runs only if a score of the tile
-        // lies more than 2^tau above it
-        if (k == 0) {
+        // The running maximum starts at the largest of rows 0, 32, 64 and 96
+        // (-inf where all four are masked): any value that some score
+        // reaches is a valid reference, and the exact reduction below runs
+        // only if a score of the tile lies more than 2^tau above it.
+        if (lane == 0) {
 #pragma unroll
           for (int h4 = 0; h4 < 8; ++h4)
-            *reinterpret_cast<float4*>(m_run + hb + 4 * h4) =
+            *reinterpret_cast<float4*>(red + quad * 64 + hb + 4 * h4) =
                 make_float4(s[4 * h4], s[4 * h4 + 1], s[4 * h4 + 2], s[4 * h4 + 3]);
         }
         softmax_sync();
-      }
-      // does any score exceed its head's running maximum by more than 2^tau?
-      float excess = -INFINITY;
-      if (valid) {
+#pragma unroll
+        for (int h4 = 0; h4 < 8; ++h4) {
+          float4 m4 = *reinterpret_cast<const float4*>(red + hb + 4 * h4);
+#pragma unroll
+          for (int qd = 1; qd < 4; ++qd) {
+            const float4 r4 = *reinterpret_cast<const float4*>(red + qd * 64 + hb + 4 * h4);
+            m4 = make_float4(fmaxf(m4.x, r4.x), fmaxf(m4.y, r4.y), fmaxf(m4.z, r4.z), fmaxf(m4.w, r4.w));
+          }
+          if (quad == 0 && lane == 0) *reinterpret_cast<float4*>(m_run + hb + 4 * h4) = m4;
+          if (valid)
+            excess = fmaxf(excess, fmaxf(fmaxf(s[4 * h4] - m4.x, s[4 * h4 + 1] - m4.y),
+                                         fmaxf(s[4 * h4 + 2] - m4.z, s[4 * h4 + 3] - m4.w)));
+        }
+      } else if (valid) {
 #pragma unroll
         for (int h4 = 0; h4 < 8; ++h4) {
           const float4 m4 = *reinterpret_cast<const float4*>(m_run + hb + 4 * h4);
@@ -940,6 +971,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
                                        fmaxf(s[4 * h4 + 2] - m4.z, s[4 * h4 + 3] - m4.w)));
         }
       }
+      // (the barrier below also publishes the first tile's m_run)
       const bool slow = softmax_sync_or(excess > kTau);
       if (tid == kSoftmax0 && i < 2) NVMLA_TRACE_POINT(101 + 10 * i);
       // (PV of the previous tile has finished: waited for before the V copy)
