@@ -950,20 +950,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
                 make_float4(s[4 * h4], s[4 * h4 + 1], s[4 * h4 + 2], s[4 * h4 + 3]);
         }
         softmax_sync();
-#pragma unroll
-        for (int h4 = 0; h4 < 8; ++h4) {
-          float4 m4 = *reinterpret_cast<const float4*>(red + hb + 4 * h4);
-#pragma unroll
-          for (int qd = 1; qd < 4; ++qd) {
-            const float4 r4 = *reinterpret_cast<const float4*>(red + qd * 64 + hb + 4 * h4);
-            m4 = make_float4(fmaxf(m4.x, r4.x), fmaxf(m4.y, r4.y), fmaxf(m4.z, r4.z), fmaxf(m4.w, r4.w));
-          }
-          if (quad == 0 && lane == 0) *reinterpret_cast<float4*>(m_run + hb + 4 * h4) = m4;
-          if (valid)
-            excess = fmaxf(excess, fmaxf(fmaxf(s[4 * h4] - m4.x, s[4 * h4 + 1] - m4.y),
-                                         fmaxf(s[4 * h4 + 2] - m4.z, s[4 * h4 + 3] - m4.w)));
+        if (quad == 0) {
+          const int h = hb + lane;
+          m_run[h] = fmaxf(fmaxf(red[h], red[64 + h]), fmaxf(red[128 + h], red[192 + h]));
         }
-      } else if (valid) {
+        softmax_sync();
+      }
+      if (valid) {
 #pragma unroll
         for (int h4 = 0; h4 < 8; ++h4) {
           const float4 m4 = *reinterpret_cast<const float4*>(m_run + hb + 4 * h4);
