@@ -758,7 +758,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
     // warps of its sub-partition, so one issuer alone cannot keep the tensor
     // core busy; the two streams touch different accumulators and are
     // ordered only through the barriers. One wait before each batch, one
-    // commit after it, straight-line loops in between.
+    // commit after it, fully unrolled straight-line MMA sequences in between
+    // (a loop branch between MMAs costs issue time).
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_f16(false, false);
       constexpr uint32_t idesc_pv = idesc_f16(true, true);
@@ -766,13 +767,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
       const uint32_t ring = tmem + kColK;
       bool mok = *abort_flag == 0;
       if (warp == kPvWarp) {
-        // (the last tile's PV also reports each block, so that the epilogue
-        // can start on it; a separate copy, as a conditional branch between
-        // MMAs costs the issue)
-        // (block j reads V chunks j and j + 4; after blocks 0-1 the next
-        // tile's V copy may start on chunks 0, 1, 4, 5)
+        // Block j reads V chunks j and j + 4: after blocks 0-1 the next
+        // tile's V copy may start on chunks 0, 1, 4, 5. The last tile's PV
+        // reports each block instead, so that the epilogue can start on it
+        // (a separate copy of the sequence: a conditional branch between
+        // MMAs costs issue time).
         auto issue_pv = [&](int i) {
-#pragma unroll 1
+#pragma unroll
           for (int j = 0; j < 2; ++j) {
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)
@@ -780,7 +781,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
                       sdesc(rb + 2048 * ks, 8192, 1024), idesc_pv, (i | ks) != 0);
           }
           mma_commit(bar(kBarPVHalf));
-#pragma unroll 1
+#pragma unroll
           for (int j = 2; j < 4; ++j) {
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)
@@ -790,7 +791,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
           mma_commit(bar(kBarPVDone));
         };
         auto issue_pv_last = [&](int i) {
-#pragma unroll 1
+#pragma unroll
           for (int j = 0; j < 4; ++j) {
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)
@@ -819,7 +820,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
           tc_fence_after();
           if (i < 2) NVMLA_TRACE_POINT(50 + 8 * i);
           // batch A: uses 0..5 (slot u, query chunk 4 (u & 1) + u / 2)
-#pragma unroll 1
+#pragma unroll
           for (int u = 0; u < 6; ++u) {
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
@@ -833,7 +834,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
           tc_fence_after();
           if (i < 2) NVMLA_TRACE_POINT(54 + 8 * i);
           // batch B: uses 6, 7 (latent chunks 3, 7) in slots 0, 1; use 8 (RoPE) in slot 2
-#pragma unroll 1
+#pragma unroll
           for (int u = 0; u < 3; ++u) {
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
