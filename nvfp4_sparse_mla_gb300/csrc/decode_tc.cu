@@ -1188,11 +1188,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
     wait_bar_warp(bar(kBarRx), 0, abort_flag, p.err_word);
     __syncthreads();
     if (tid == 0) NVMLA_TRACE_POINT(43);
-    // item = (head group u, dim row dl): lanes take consecutive dims; the
-    // bf16 results go to [64 heads][D dims] in the latent tile's space (its
-    // bulk stores have completed), then to out in 8-byte pieces
+    // item = (head group u, dim row dl): lanes take consecutive dims
     const uint8_t* rxp = smem + kOffQ;
-    __nv_bfloat16* ostg = reinterpret_cast<__nv_bfloat16*>(smem + kOffL);
     for (int it = tid; it < D * 8; it += kThreads) {
       const int u = it / D, dl = it - u * D, d = d0 + dl;
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -1210,16 +1207,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
           acc[2 * e + 1] += c[2 * e + 1] * f.y;
         }
       }
+      // straight to out: the lanes of a warp write consecutive dims of a head
+      __nv_bfloat16* o = p.out + (static_cast<int64_t>(t) * p.H + h0 + 8 * u) * kLatent + d;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) ostg[(8 * u + e) * D + dl] = __float2bfloat16_rn(acc[e]);
-    }
-    __syncthreads();
-    if (tid == 0) NVMLA_TRACE_POINT(46);
-    const int per_head = D / 4;
-    for (int pc = tid; pc < kHeads * per_head; pc += kThreads) {
-      const int h = pc / per_head, g = pc - h * per_head;
-      const uint2 v = *reinterpret_cast<const uint2*>(ostg + h * D + 4 * g);
-      *reinterpret_cast<uint2*>(p.out + (static_cast<int64_t>(t) * p.H + h0 + h) * kLatent + d0 + 4 * g) = v;
+      for (int e = 0; e < 8; ++e) o[e * kLatent] = __float2bfloat16_rn(acc[e]);
     }
   }
   if (tid == 0) NVMLA_TRACE_POINT(44);
