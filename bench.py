@@ -49,6 +49,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-staged", action="store_true")
+    ap.add_argument("--no-layered", action="store_true")
     return ap.parse_args()
 
 
@@ -463,6 +464,43 @@ def main():
                   "dequant_us": statistics.mean(s1) * 1e3, "attend_us": statistics.mean(s2) * 1e3,
                   "fp8_buffer_bytes": w.T * w.topk * 576}
 
+    # ---------------- the same decode over one layer of a block-major cache
+    # of 4 layers (the rows of this workload in layer 2); same protocol
+    layered = None
+    if not args.no_layered:
+        n_layers, layer = 4, 2
+        lcache = torch.zeros((cache.shape[0], n_layers, 64, 352), dtype=torch.uint8, device=dev)
+        lcache[:, layer] = cache
+        lo, ll = torch.empty_like(out), torch.empty_like(lse)
+
+        def layered_call():
+            nvmla.sparse_mla_decode_layered(ql, qr, lcache, layer, bt, tk, w.sm_scale, out=lo, lse=ll, q_seq_idx=qs,
+                                            seq_lens=sl, workspace=ws, impl=impl)
+
+        decode()
+        for _ in range(3):
+            flush.fill_(1.0)
+            layered_call()
+        torch.cuda.synchronize()
+        same = bool(torch.equal(lo, out) and torch.equal(ll, lse))
+        if not same:
+            raise RuntimeError("the layered decode differs from the one-layer decode of the same rows")
+        lev = []
+        for k in range(K):
+            if k % GROUP == 0:
+                torch.cuda._sleep(LEAD_CYCLES_PER_STEP * min(GROUP, K - k))
+            flush.fill_(float(k))
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            e[0].record()
+            layered_call()
+            e[1].record()
+            lev.append(e)
+        torch.cuda.synchronize()
+        layered = {"us_per_call": statistics.mean([e[0].elapsed_time(e[1]) for e in lev]) * 1e3,
+                   "num_layers": n_layers, "layer": layer, "cache_bytes": lcache.numel(),
+                   "bitwise_equal_to_one_layer_decode": same}
+        del lcache
+
     # ---------------- pack of the write+read workload's 6144-token chunk
     plat, prope, pslots = workloads.pack_chunk(seed=4, n=6144, num_pages=2188)
     pcache = torch.zeros((2188, 64, 352), dtype=torch.uint8, device=dev)
@@ -523,6 +561,7 @@ def main():
         "pack_chunk": {"tokens": 6144, "us_per_call": pack_us, "gbs": pack_bytes / (pack_us * 1e-6) / 1e9,
                        "frac_hbm": pack_bytes / (pack_us * 1e-6) / 1e9 / bw},
         "staged": staged,
+        "layered": layered,
         "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "how": "per step: one host-to-device copy of every input from pinned memory, nvfp4_mla_pack, "
                        "sparse_mla_decode, one device-to-host copy of out and lse, replayed as a CUDA graph; "

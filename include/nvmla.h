@@ -195,6 +195,47 @@ size_t sparse_mla_decode_workspace_size_ex(int32_t T, int32_t H, int32_t topk,
                                            const nvmla_decode_options* opts);
 
 /*
+ * Block-major multi-layer caches.
+ * [Serving, "Changing the layout to reduce fragmentation": a block-major
+ * layout keeps one block's data for several layers together, so that moving
+ * KV between workers takes fewer, larger copies; "KV cache and data
+ * transfer" on the [KV] page: 64-token blocks]. The layout the pages name
+ * (block, layer, head, token, channel) is read here, for the single latent
+ * "head" of MLA, as
+ *
+ *   cache  (device) uint8 [num_blocks][num_layers][64][352], 32-byte aligned:
+ *          row (b, l, i) at byte ((b * num_layers + l) * 64 + i) * 352.
+ *
+ * The calls below read or write one layer of such a cache. Slots and block
+ * tables mean what they mean for a one-layer cache (slot = block * 64 + i),
+ * so one block table serves every layer; num_blocks takes num_pages' place
+ * in every check. A one-layer cache is num_layers = 1, layer = 0, and then
+ * these calls are nvfp4_mla_pack and sparse_mla_decode_ex. Arguments,
+ * errors and results otherwise as there; in addition
+ * NVMLA_ERR_INVALID_ARG unless 1 <= num_layers <= 4096 and
+ * 0 <= layer < num_layers.
+ */
+nvmla_status nvfp4_mla_pack_layered(const void* latent_bf16, int64_t latent_stride,
+                                    const void* rope_bf16, int64_t rope_stride,
+                                    const int32_t* slot_mapping, int64_t n_tokens,
+                                    uint8_t* cache, int64_t num_blocks,
+                                    int32_t num_layers, int32_t layer,
+                                    int32_t* err_word, nvmla_stream_t stream);
+
+nvmla_status sparse_mla_decode_layered(const void* q_latent, const void* q_rope,
+                                       const uint8_t* cache, int64_t num_blocks,
+                                       int32_t num_layers, int32_t layer,
+                                       const int32_t* block_table, int32_t num_seqs,
+                                       int32_t max_pages_per_seq,
+                                       const int32_t* topk_idx, int32_t topk,
+                                       const int32_t* q_seq_idx, const int32_t* seq_lens,
+                                       int32_t T, int32_t H, float sm_scale,
+                                       void* out, float* lse,
+                                       void* workspace, size_t workspace_bytes,
+                                       int32_t* err_word, const nvmla_decode_options* opts,
+                                       nvmla_stream_t stream);
+
+/*
  * sparse_mla_decode_noalloc -- sparse_mla_decode without a workspace
  * argument. The pages describe no such call: it exists for callers that
  * cannot allocate GPU memory (an engine whose memory pool owns the whole

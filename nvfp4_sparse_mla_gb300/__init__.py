@@ -13,6 +13,9 @@ Calls (same names as the C ABI, see include/nvmla.h):
 * ``sparse_mla_decode(q_latent, q_rope, cache, block_table, topk_idx, sm_scale, ...)``
 * ``sparse_mla_decode_noalloc(q_latent, q_rope, cache, block_table, topk_idx, sm_scale, out, lse, ...)``
   (the same decode with the library's own split scratch; allocates nothing)
+* ``nvfp4_mla_pack_layered(latent, rope, slot_mapping, cache, layer)`` and
+  ``sparse_mla_decode_layered(q_latent, q_rope, cache, layer, block_table, topk_idx, sm_scale, ...)``
+  (one layer of a block-major multi-layer cache [num_blocks, num_layers, 64, 352])
 * ``nvfp4_stage_dequant_fp8(cache, block_table, topk_idx, ...)`` and
   ``sparse_mla_decode_fp8rows(q_latent, q_rope, fp8_rows, row_idx, sm_scale, ...)``
   (the staged baseline)
@@ -29,6 +32,7 @@ __all__ = [
     "NvmlaError", "nvfp4_mla_pack", "sparse_mla_decode", "sparse_mla_decode_workspace_size", "sparse_mla_decode_fp8rows_workspace_size", "launch_count",
     "nvfp4_stage_dequant_fp8", "sparse_mla_decode_fp8rows", "library_path", "load",
     "sparse_mla_decode_noalloc", "sparse_mla_decode_noalloc_max_scratch",
+    "nvfp4_mla_pack_layered", "sparse_mla_decode_layered",
     "IMPL_AUTO", "IMPL_MMA", "IMPL_TCGEN05", "ROW_BYTES", "FP8_ROW_BYTES", "PAGE_TOKENS",
 ]
 
@@ -74,6 +78,9 @@ def load():
         "nvfp4_mla_pack": (I32, [P, I64, P, I64, P, I64, P, I64, P, P]),
         "sparse_mla_decode": (I32, [P, P, P, I64, P, I32, I32, P, I32, P, P, I32, I32, F, P, P, P, SZ, P, P]),
         "sparse_mla_decode_ex": (I32, [P, P, P, I64, P, I32, I32, P, I32, P, P, I32, I32, F, P, P, P, SZ, P, OPT, P]),
+        "nvfp4_mla_pack_layered": (I32, [P, I64, P, I64, P, I64, P, I64, I32, I32, P, P]),
+        "sparse_mla_decode_layered": (I32, [P, P, P, I64, I32, I32, P, I32, I32, P, I32, P, P, I32, I32, F, P, P, P, SZ,
+                                            P, OPT, P]),
         "sparse_mla_decode_workspace_size": (SZ, [I32, I32, I32]),
         "sparse_mla_decode_workspace_size_ex": (SZ, [I32, I32, I32, OPT]),
         "sparse_mla_decode_noalloc": (I32, [P, P, P, I64, P, I32, I32, P, I32, P, P, I32, I32, F, P, P, P, P]),
@@ -158,6 +165,83 @@ def nvfp4_mla_pack(latent: torch.Tensor, rope: torch.Tensor, slot_mapping: torch
     _check(lib.nvfp4_mla_pack(_ptr(latent), ls, _ptr(rope), rs, _ptr(slot_mapping), n,
                               _ptr(cache), cache.shape[0], _ptr(err_word), _stream(cache, stream)))
     return cache
+
+
+def _layered_cache(cache: torch.Tensor, layer: int):
+    _need(cache, "cache", torch.uint8, 4)
+    if cache.shape[2:] != (PAGE_TOKENS, ROW_BYTES):
+        raise ValueError("cache must be [num_blocks, num_layers, 64, 352]")
+    if not 0 <= int(layer) < cache.shape[1]:
+        raise ValueError(f"layer {layer} outside [0, {cache.shape[1]})")
+
+
+def nvfp4_mla_pack_layered(latent: torch.Tensor, rope: torch.Tensor, slot_mapping: torch.Tensor, cache: torch.Tensor,
+                           layer: int, err_word: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """nvfp4_mla_pack into layer `layer` of a block-major multi-layer cache
+    [num_blocks, num_layers, 64, 352] (uint8); slots are block * 64 + token
+    as for a one-layer cache. Returns cache."""
+    _need(latent, "latent", torch.bfloat16, 2, contiguous=False)
+    _need(rope, "rope", torch.bfloat16, 2, contiguous=False)
+    _need(slot_mapping, "slot_mapping", torch.int32, 1)
+    _layered_cache(cache, layer)
+    if latent.shape[1] != 512 or rope.shape[1] != 64 or latent.stride(1) != 1 or rope.stride(1) != 1:
+        raise ValueError("latent must be [N, 512] and rope [N, 64] with unit inner stride")
+    n = latent.shape[0]
+    if rope.shape[0] != n or slot_mapping.shape[0] != n:
+        raise ValueError("latent, rope and slot_mapping must have the same number of tokens")
+    if err_word is not None:
+        _need(err_word, "err_word", torch.int32, 1)
+    lib = load()
+    ls = latent.stride(0) if n > 1 else 512
+    rs = rope.stride(0) if n > 1 else 64
+    _check(lib.nvfp4_mla_pack_layered(_ptr(latent), ls, _ptr(rope), rs, _ptr(slot_mapping), n, _ptr(cache),
+                                      cache.shape[0], cache.shape[1], int(layer), _ptr(err_word),
+                                      _stream(cache, stream)))
+    return cache
+
+
+def sparse_mla_decode_layered(q_latent: torch.Tensor, q_rope: torch.Tensor, cache: torch.Tensor, layer: int,
+                              block_table: torch.Tensor, topk_idx: torch.Tensor, sm_scale: float,
+                              out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                              q_seq_idx: Optional[torch.Tensor] = None, seq_lens: Optional[torch.Tensor] = None,
+                              workspace: Optional[torch.Tensor] = None, err_word: Optional[torch.Tensor] = None,
+                              impl=None, num_splits=None, stream=None):
+    """sparse_mla_decode over layer `layer` of a block-major multi-layer cache
+    [num_blocks, num_layers, 64, 352]. Returns (out, lse)."""
+    _need(q_latent, "q_latent", torch.bfloat16, 3)
+    _need(q_rope, "q_rope", torch.bfloat16, 3)
+    _layered_cache(cache, layer)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(topk_idx, "topk_idx", torch.int32, 2)
+    T, H, dl = q_latent.shape
+    if dl != 512 or tuple(q_rope.shape) != (T, H, 64):
+        raise ValueError("q_latent must be [T, H, 512] and q_rope [T, H, 64]")
+    if topk_idx.shape[0] != T:
+        raise ValueError("topk_idx must be [T, topk]")
+    if q_seq_idx is not None:
+        _need(q_seq_idx, "q_seq_idx", torch.int32, 1)
+    if seq_lens is not None:
+        _need(seq_lens, "seq_lens", torch.int32, 1)
+    if out is None:
+        out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=q_latent.device)
+    if lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=q_latent.device)
+    _need(out, "out", torch.bfloat16, 3)
+    _need(lse, "lse", torch.float32, 2)
+    topk = topk_idx.shape[1]
+    opts = _opts(impl, num_splits)
+    lib = load()
+    if workspace is None:
+        nbytes = int(lib.sparse_mla_decode_workspace_size_ex(T, H, topk, opts))
+        if nbytes:
+            workspace = torch.empty(nbytes, dtype=torch.uint8, device=q_latent.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.sparse_mla_decode_layered(_ptr(q_latent), _ptr(q_rope), _ptr(cache), cache.shape[0], cache.shape[1],
+                                         int(layer), _ptr(block_table), block_table.shape[0], block_table.shape[1],
+                                         _ptr(topk_idx), topk, _ptr(q_seq_idx), _ptr(seq_lens), T, H,
+                                         float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
+                                         _ptr(err_word), opts, _stream(q_latent, stream)))
+    return out, lse
 
 
 def sparse_mla_decode_workspace_size(T: int, H: int, topk: int, impl=None, num_splits=None) -> int:

@@ -13,7 +13,7 @@
 namespace nvmla {
 
 cudaError_t launch_pack(const void*, int64_t, const void*, int64_t, const int32_t*, int64_t, uint8_t*, int64_t,
-                        int32_t*, cudaStream_t);
+                        int32_t, int32_t*, cudaStream_t);
 cudaError_t launch_stage_dequant(const uint8_t*, const RowSelect&, int, uint8_t*, int32_t*, int32_t*,
                                  cudaStream_t);
 cudaError_t launch_decode_mma(int fmt, const void*, const void*, const uint8_t*, const RowSelect&,
@@ -107,6 +107,21 @@ nvmla_status check_cache(const uint8_t* cache, int64_t num_pages, const int32_t*
   return NVMLA_OK;
 }
 
+// A layer of a block-major multi-layer cache ([num_blocks][num_layers][64]
+// rows): its rows start layer * 64 rows in, and blocks lie 64 * num_layers
+// rows apart. One layer per cache is num_layers = 1, layer = 0.
+constexpr int32_t kMaxLayers = 4096;
+nvmla_status check_layers(int64_t num_blocks, int32_t num_layers, int32_t layer) {
+  if (num_layers < 1 || num_layers > kMaxLayers)
+    return fail(NVMLA_ERR_INVALID_ARG, "num_layers = %d must be in [1, %d]", num_layers, kMaxLayers);
+  if (layer < 0 || layer >= num_layers)
+    return fail(NVMLA_ERR_INVALID_ARG, "layer = %d must be in [0, num_layers = %d)", layer, num_layers);
+  if (num_blocks >= (int64_t{1} << 40) / num_layers)
+    return fail(NVMLA_ERR_UNSUPPORTED, "num_blocks * num_layers too large");
+  return NVMLA_OK;
+}
+int64_t layer_offset(int32_t layer) { return static_cast<int64_t>(layer) * NVMLA_PAGE_TOKENS * NVMLA_ROW_BYTES; }
+
 int pick_impl(const nvmla_decode_options* opts, int H) {
   const int want = opts ? opts->impl : NVMLA_IMPL_AUTO;
   if (want == NVMLA_IMPL_MMA) return NVMLA_IMPL_MMA;
@@ -189,9 +204,10 @@ int32_t nvmla_version(void) { return 100; }
 
 uint64_t nvmla_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
-nvmla_status nvfp4_mla_pack(const void* latent_bf16, int64_t latent_stride, const void* rope_bf16,
-                            int64_t rope_stride, const int32_t* slot_mapping, int64_t n_tokens, uint8_t* cache,
-                            int64_t num_pages, int32_t* err_word, nvmla_stream_t stream) {
+namespace {
+nvmla_status pack_impl(const void* latent_bf16, int64_t latent_stride, const void* rope_bf16, int64_t rope_stride,
+                       const int32_t* slot_mapping, int64_t n_tokens, uint8_t* cache, int64_t num_blocks,
+                       int32_t num_layers, int32_t layer, int32_t* err_word, nvmla_stream_t stream) {
   if (n_tokens < 0) return fail(NVMLA_ERR_INVALID_ARG, "n_tokens = %lld must be >= 0", (long long)n_tokens);
   if (n_tokens == 0) return NVMLA_OK;
   if (!latent_bf16 || !rope_bf16 || !slot_mapping || !cache)
@@ -202,11 +218,30 @@ nvmla_status nvfp4_mla_pack(const void* latent_bf16, int64_t latent_stride, cons
     return fail(NVMLA_ERR_INVALID_ARG, "rope must be 4-byte aligned with an even stride >= 64");
   if (!aligned(slot_mapping, 4)) return fail(NVMLA_ERR_INVALID_ARG, "slot_mapping must be 4-byte aligned");
   if (!aligned(cache, 32)) return fail(NVMLA_ERR_INVALID_ARG, "cache must be 32-byte aligned");
-  if (num_pages < 1) return fail(NVMLA_ERR_INVALID_ARG, "num_pages must be >= 1");
+  if (num_blocks < 1) return fail(NVMLA_ERR_INVALID_ARG, "num_pages = %lld must be >= 1", (long long)num_blocks);
+  nvmla_status s = check_layers(num_blocks, num_layers, layer);
+  if (s != NVMLA_OK) return s;
   if (err_word && !aligned(err_word, 4)) return fail(NVMLA_ERR_INVALID_ARG, "err_word must be 4-byte aligned");
-  return counted(launch_pack(latent_bf16, latent_stride, rope_bf16, rope_stride, slot_mapping, n_tokens, cache,
-                             num_pages, err_word, reinterpret_cast<cudaStream_t>(stream)),
+  return counted(launch_pack(latent_bf16, latent_stride, rope_bf16, rope_stride, slot_mapping, n_tokens,
+                             cache + layer_offset(layer), num_blocks, NVMLA_PAGE_TOKENS * num_layers, err_word,
+                             reinterpret_cast<cudaStream_t>(stream)),
                  1, "nvfp4_mla_pack launch");
+}
+}  // namespace
+
+nvmla_status nvfp4_mla_pack(const void* latent_bf16, int64_t latent_stride, const void* rope_bf16,
+                            int64_t rope_stride, const int32_t* slot_mapping, int64_t n_tokens, uint8_t* cache,
+                            int64_t num_pages, int32_t* err_word, nvmla_stream_t stream) {
+  return pack_impl(latent_bf16, latent_stride, rope_bf16, rope_stride, slot_mapping, n_tokens, cache, num_pages, 1, 0,
+                   err_word, stream);
+}
+
+nvmla_status nvfp4_mla_pack_layered(const void* latent_bf16, int64_t latent_stride, const void* rope_bf16,
+                                    int64_t rope_stride, const int32_t* slot_mapping, int64_t n_tokens,
+                                    uint8_t* cache, int64_t num_blocks, int32_t num_layers, int32_t layer,
+                                    int32_t* err_word, nvmla_stream_t stream) {
+  return pack_impl(latent_bf16, latent_stride, rope_bf16, rope_stride, slot_mapping, n_tokens, cache, num_blocks,
+                   num_layers, layer, err_word, stream);
 }
 
 size_t sparse_mla_decode_workspace_size_ex(int32_t T, int32_t H, int32_t topk, const nvmla_decode_options* opts) {
@@ -235,21 +270,24 @@ size_t sparse_mla_decode_fp8rows_workspace_size(int32_t T, int32_t H, int32_t to
   return workspace_bytes(impl, T, H, s);
 }
 
-nvmla_status sparse_mla_decode_ex(const void* q_latent, const void* q_rope, const uint8_t* cache, int64_t num_pages,
-                                  const int32_t* block_table, int32_t num_seqs, int32_t max_pages_per_seq,
-                                  const int32_t* topk_idx, int32_t topk, const int32_t* q_seq_idx,
-                                  const int32_t* seq_lens, int32_t T, int32_t H, float sm_scale, void* out,
-                                  float* lse, void* workspace, size_t workspace_bytes, int32_t* err_word,
-                                  const nvmla_decode_options* opts, nvmla_stream_t stream) {
+namespace {
+nvmla_status decode_impl(const void* q_latent, const void* q_rope, const uint8_t* cache, int64_t num_blocks,
+                         int32_t num_layers, int32_t layer, const int32_t* block_table, int32_t num_seqs,
+                         int32_t max_pages_per_seq, const int32_t* topk_idx, int32_t topk, const int32_t* q_seq_idx,
+                         const int32_t* seq_lens, int32_t T, int32_t H, float sm_scale, void* out, float* lse,
+                         void* workspace, size_t workspace_bytes, int32_t* err_word,
+                         const nvmla_decode_options* opts, nvmla_stream_t stream) {
   nvmla_status s = check_shape(T, H, topk, sm_scale);
   if (s != NVMLA_OK || T == 0) return s;
   if ((s = check_queries(q_latent, q_rope, out, lse)) != NVMLA_OK) return s;
-  if ((s = check_cache(cache, num_pages, block_table, num_seqs, max_pages_per_seq, topk_idx)) != NVMLA_OK) return s;
+  if ((s = check_cache(cache, num_blocks, block_table, num_seqs, max_pages_per_seq, topk_idx)) != NVMLA_OK) return s;
+  if ((s = check_layers(num_blocks, num_layers, layer)) != NVMLA_OK) return s;
   if (err_word && !aligned(err_word, 4)) return fail(NVMLA_ERR_INVALID_ARG, "err_word must be 4-byte aligned");
   if (opts && (opts->impl < 0 || opts->impl > NVMLA_IMPL_TCGEN05 || opts->num_splits < 0))
     return fail(NVMLA_ERR_INVALID_ARG, "bad options");
-  RowSelect sel{topk_idx, block_table, q_seq_idx, seq_lens, num_pages * NVMLA_PAGE_TOKENS, topk, max_pages_per_seq,
-                num_seqs};
+  RowSelect sel{topk_idx, block_table, q_seq_idx, seq_lens, num_blocks * NVMLA_PAGE_TOKENS, topk, max_pages_per_seq,
+                num_seqs, NVMLA_PAGE_TOKENS * num_layers};
+  const uint8_t* rows = cache + layer_offset(layer);
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int impl = pick_impl(opts, H);
   if (impl == NVMLA_IMPL_TCGEN05 && !tc_supported(H))
@@ -257,13 +295,37 @@ nvmla_status sparse_mla_decode_ex(const void* q_latent, const void* q_rope, cons
   int splits = 1;
   if ((s = pick_splits(impl, opts, T, H, topk, workspace_bytes, workspace, &splits)) != NVMLA_OK) return s;
   if (impl == NVMLA_IMPL_TCGEN05) {
-    return counted(launch_decode_tc(0, q_latent, q_rope, cache, sel, nullptr, T, H, topk, sm_scale, out, lse,
+    return counted(launch_decode_tc(0, q_latent, q_rope, rows, sel, nullptr, T, H, topk, sm_scale, out, lse,
                                     workspace, splits, err_word, st),
                    1, "sparse_mla_decode (tcgen05) launch");
   }
-  return counted(launch_decode_mma(0, q_latent, q_rope, cache, sel, nullptr, T, H, topk, sm_scale, out, lse,
+  return counted(launch_decode_mma(0, q_latent, q_rope, rows, sel, nullptr, T, H, topk, sm_scale, out, lse,
                                    workspace, splits, err_word, st),
                  splits > 1 ? 2 : 1, "sparse_mla_decode (mma) launch");
+}
+}  // namespace
+
+nvmla_status sparse_mla_decode_ex(const void* q_latent, const void* q_rope, const uint8_t* cache, int64_t num_pages,
+                                  const int32_t* block_table, int32_t num_seqs, int32_t max_pages_per_seq,
+                                  const int32_t* topk_idx, int32_t topk, const int32_t* q_seq_idx,
+                                  const int32_t* seq_lens, int32_t T, int32_t H, float sm_scale, void* out,
+                                  float* lse, void* workspace, size_t workspace_bytes, int32_t* err_word,
+                                  const nvmla_decode_options* opts, nvmla_stream_t stream) {
+  return decode_impl(q_latent, q_rope, cache, num_pages, 1, 0, block_table, num_seqs, max_pages_per_seq, topk_idx,
+                     topk, q_seq_idx, seq_lens, T, H, sm_scale, out, lse, workspace, workspace_bytes, err_word, opts,
+                     stream);
+}
+
+nvmla_status sparse_mla_decode_layered(const void* q_latent, const void* q_rope, const uint8_t* cache,
+                                       int64_t num_blocks, int32_t num_layers, int32_t layer,
+                                       const int32_t* block_table, int32_t num_seqs, int32_t max_pages_per_seq,
+                                       const int32_t* topk_idx, int32_t topk, const int32_t* q_seq_idx,
+                                       const int32_t* seq_lens, int32_t T, int32_t H, float sm_scale, void* out,
+                                       float* lse, void* workspace, size_t workspace_bytes, int32_t* err_word,
+                                       const nvmla_decode_options* opts, nvmla_stream_t stream) {
+  return decode_impl(q_latent, q_rope, cache, num_blocks, num_layers, layer, block_table, num_seqs, max_pages_per_seq,
+                     topk_idx, topk, q_seq_idx, seq_lens, T, H, sm_scale, out, lse, workspace, workspace_bytes,
+                     err_word, opts, stream);
 }
 
 nvmla_status sparse_mla_decode(const void* q_latent, const void* q_rope, const uint8_t* cache, int64_t num_pages,
@@ -289,7 +351,7 @@ nvmla_status nvfp4_stage_dequant_fp8(const uint8_t* cache, int64_t num_pages, co
   if (!aligned(fp8_rows, 16) || !aligned(row_idx, 4)) return fail(NVMLA_ERR_INVALID_ARG, "fp8_rows must be 16-byte aligned");
   if (err_word && !aligned(err_word, 4)) return fail(NVMLA_ERR_INVALID_ARG, "err_word must be 4-byte aligned");
   RowSelect sel{topk_idx, block_table, q_seq_idx, seq_lens, num_pages * NVMLA_PAGE_TOKENS, topk, max_pages_per_seq,
-                num_seqs};
+                num_seqs, NVMLA_PAGE_TOKENS};
   return counted(launch_stage_dequant(cache, sel, T, fp8_rows, row_idx, err_word, reinterpret_cast<cudaStream_t>(stream)),
                  1, "nvfp4_stage_dequant_fp8 launch");
 }

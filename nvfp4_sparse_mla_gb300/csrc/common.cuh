@@ -100,6 +100,14 @@ __device__ __forceinline__ void report_error(int32_t* err_word, int32_t flag, in
   }
 }
 
+// Byte offset of the row of cache slot s (block s / 64, token s % 64) when
+// consecutive blocks lie page_rows rows apart: 64 for a cache that holds one
+// layer, 64 L when each block keeps the rows of L layers together
+// (block-major, layer-next: the layer's own rows then start at layer * 64).
+__host__ __device__ __forceinline__ int64_t cache_row_offset(int64_t s, int32_t page_rows) {
+  return ((s >> 6) * page_rows + (s & 63)) * kRowBytes;
+}
+
 // Physical cache slot of slot k of query token t, or -1 (padding or a bad
 // entry; bad entries are reported once, by the caller's choice of thread).
 // A token whose sequence index lies outside [0, num_seqs) has no valid slot.
@@ -112,6 +120,7 @@ struct RowSelect {
   int32_t topk;
   int32_t max_pages;
   int32_t num_seqs;
+  int32_t page_rows;  // rows from one block to the next (cache_row_offset)
 
   __device__ __forceinline__ int64_t slot(int t, int k, int32_t* err_word, bool report) const {
     const int32_t p = __ldg(topk_idx + static_cast<int64_t>(t) * topk + k);

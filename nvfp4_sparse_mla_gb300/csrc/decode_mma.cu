@@ -189,7 +189,11 @@ __global__ void __launch_bounds__(kMmaThreads, 1) decode_mma_kernel(MmaParams p)
     for (int c = tid; c < n * kChunks; c += kMmaThreads) {
       const int r = c / kChunks, q = c % kChunks;
       const int32_t row = rows[base + r];
-      if (row >= 0) cp_async_16(dst + r * kRaw + q * 16, p.cache + static_cast<int64_t>(row) * kRaw + q * 16);
+      if (row >= 0) {
+        const int64_t off = FMT == kNvfp4Paged ? cache_row_offset(row, p.sel.page_rows)
+                                               : static_cast<int64_t>(row) * kRaw;
+        cp_async_16(dst + r * kRaw + q * 16, p.cache + off + q * 16);
+      }
     }
   };
 

@@ -611,14 +611,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
   uint32_t rr[16];    // the 64 RoPE bytes (half 0 only)
   int32_t slot0 = -1;
   auto load_codes = [&](int32_t slot, int j) {
-    if (slot >= 0) ldg_nc_v8(p.cache + static_cast<int64_t>(slot) * kRowBytes + 128 * uh + 32 * j, rc[j]);
+    if (slot >= 0) ldg_nc_v8(p.cache + cache_row_offset(slot, p.sel.page_rows) + 128 * uh + 32 * j, rc[j]);
   };
   auto load_scale = [&](int32_t slot) {
-    if (slot >= 0) rs = ldg_nc_v4(p.cache + static_cast<int64_t>(slot) * kRowBytes + kScaleOff + 16 * uh);
+    if (slot >= 0) rs = ldg_nc_v4(p.cache + cache_row_offset(slot, p.sel.page_rows) + kScaleOff + 16 * uh);
   };
   auto load_rope = [&](int32_t slot) {
     if (slot >= 0 && uh == 0) {
-      const uint8_t* row = p.cache + static_cast<int64_t>(slot) * kRowBytes;
+      const uint8_t* row = p.cache + cache_row_offset(slot, p.sel.page_rows);
       ldg_nc_v8(row + kRopeOff, rr);
       ldg_nc_v8(row + kRopeOff + 32, rr + 8);
     }
@@ -860,7 +860,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
     // (requested together with them, they delay them)
     for (int i = 1 + (sj >> 7); i < ntiles; i += 2) {
       const int32_t sl = slots[i * kTile + (sj & 127)];
-      if (sl >= 0) prefetch_l2(p.cache + static_cast<int64_t>(sl) * kRowBytes, kRowBytes);
+      if (sl >= 0) prefetch_l2(p.cache + cache_row_offset(sl, p.sel.page_rows), kRowBytes);
     }
     // S^T is free for the first tile
     warp_arrive(bar(kBarKFullA), lane);

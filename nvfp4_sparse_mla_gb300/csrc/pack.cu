@@ -30,7 +30,7 @@ __global__ void __launch_bounds__(kPackWarps * 32)
 nvfp4_pack_kernel(const __nv_bfloat16* __restrict__ latent, int64_t lat_stride,
                   const __nv_bfloat16* __restrict__ rope, int64_t rope_stride,
                   const int32_t* __restrict__ slot_mapping, int64_t n_tokens,
-                  uint8_t* __restrict__ cache, int64_t num_slots, int32_t* err_word) {
+                  uint8_t* __restrict__ cache, int64_t num_slots, int32_t page_rows, int32_t* err_word) {
   __shared__ __align__(16) uint8_t rowbuf[kPackWarps][kRowBytes];
   const int lane = threadIdx.x & 31;
   const int wib = threadIdx.x >> 5;
@@ -78,7 +78,7 @@ nvfp4_pack_kernel(const __nv_bfloat16* __restrict__ latent, int64_t lat_stride,
     *reinterpret_cast<uint16_t*>(row + kRopeOff + 2 * lane) = r8;
     __syncwarp();
     if (lane < kRowBytes / 16) {
-      reinterpret_cast<uint4*>(cache + slot * kRowBytes)[lane] = reinterpret_cast<const uint4*>(row)[lane];
+      reinterpret_cast<uint4*>(cache + cache_row_offset(slot, page_rows))[lane] = reinterpret_cast<const uint4*>(row)[lane];
     }
     __syncwarp();
   }
@@ -86,12 +86,12 @@ nvfp4_pack_kernel(const __nv_bfloat16* __restrict__ latent, int64_t lat_stride,
 
 cudaError_t launch_pack(const void* latent, int64_t lat_stride, const void* rope, int64_t rope_stride,
                         const int32_t* slot_mapping, int64_t n_tokens, uint8_t* cache, int64_t num_pages,
-                        int32_t* err_word, cudaStream_t stream) {
+                        int32_t page_rows, int32_t* err_word, cudaStream_t stream) {
   const int64_t blocks_needed = (n_tokens + kPackWarps - 1) / kPackWarps;
   const int blocks = static_cast<int>(blocks_needed < 152 * 16 ? blocks_needed : 152 * 16);
   nvfp4_pack_kernel<<<blocks, kPackWarps * 32, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(latent), lat_stride, static_cast<const __nv_bfloat16*>(rope),
-      rope_stride, slot_mapping, n_tokens, cache, num_pages * kPage, err_word);
+      rope_stride, slot_mapping, n_tokens, cache, num_pages * kPage, page_rows, err_word);
   return cudaGetLastError();
 }
 

@@ -38,7 +38,7 @@ stage_dequant_kernel(const uint8_t* __restrict__ cache, RowSelect sel, int T, ui
     const int64_t slot = sel.slot(t, k, err_word, lane == 0);
     if (lane == 0) row_idx[w] = slot >= 0 ? k : -1;
     if (slot < 0) continue;
-    const uint8_t* src = cache + slot * kRowBytes;
+    const uint8_t* src = cache + cache_row_offset(slot, sel.page_rows);
     uint8_t* dst = fp8_rows + w * kFp8RowBytes;
     const uint2 c = __ldg(reinterpret_cast<const uint2*>(src) + lane);
     const uint32_t s2 = e4m3_to_f16x2_bcast(__ldg(src + kScaleOff + lane));

@@ -26,6 +26,7 @@ Modules:
 * ``pack``      -- the 352-byte cache row writer (pinned).
 * ``attention`` -- masked sparse softmax attention over selected rows (pinned).
 * ``staged``    -- the staged baseline's FP8 requantisation (pinned).
+* ``layered``   -- one layer of a block-major multi-layer cache (pinned).
 
 Every function is pinned by tests under ``tests/`` against facts the pages
 or mathematics fix (printed grid and byte counts, library conversions,

@@ -104,3 +104,31 @@ def test_workspace_size_is_host_only(lib):
     assert lib.sparse_mla_decode_workspace_size(15, 64, 2048, impl=lib.IMPL_MMA, num_splits=1) == 0
     n = lib.sparse_mla_decode_workspace_size(15, 64, 2048, impl=lib.IMPL_MMA, num_splits=8)
     assert n == 15 * 8 * 64 * 514 * 4
+
+
+def test_layered_calls_reject_bad_layers(lib):
+    L = _raw(lib)
+    P = ctypes.c_void_p
+    ok = P(0x10000)
+
+    def dec(**kw):
+        a = dict(ql=ok, qr=ok, cache=ok, blocks=10, layers=4, layer=1, bt=ok, nseq=1, maxp=4, topk_idx=ok, topk=2048,
+                 qs=None, sl=None, T=15, H=64, scale=0.1, out=ok, lse=ok, ws=None, wsb=0, err=None, opts=None,
+                 stream=None)
+        a.update(kw)
+        return L.sparse_mla_decode_layered(*a.values())
+
+    def pk(**kw):
+        a = dict(lat=ok, ls=512, rope=ok, rs=64, slots=ok, n=10, cache=ok, blocks=1, layers=4, layer=1, err=None,
+                 stream=None)
+        a.update(kw)
+        return L.nvfp4_mla_pack_layered(*a.values())
+
+    for call in (dec, pk):
+        assert call(layer=4) == 1
+        assert call(layer=-1) == 1
+        assert call(layers=0, layer=0) == 1
+        assert call(layers=5000, layer=0) == 1
+        assert call(cache=P(0x10010)) == 1      # misaligned cache
+        assert b"" != L.nvmla_last_error()
+    assert dec(T=0) == 0 and pk(n=0) == 0       # no-ops, nothing touched
