@@ -50,6 +50,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-staged", action="store_true")
     ap.add_argument("--no-layered", action="store_true")
+    ap.add_argument("--no-topk", action="store_true")
     return ap.parse_args()
 
 
@@ -501,6 +502,34 @@ def main():
                    "bitwise_equal_to_one_layer_decode": same}
         del lcache
 
+    # ---------------- the step upstream: top-2048 lists from scores of the
+    # whole context (synthetic N(0,1) scores, seeded), same protocol
+    topk_sel = None
+    if not args.no_topk:
+        gen = torch.Generator(device="cpu").manual_seed(7)
+        ctx = int(w.seq_lens[0])
+        sc = torch.randn((w.T, ctx), generator=gen, dtype=torch.float32).to(dev)
+        tko = torch.empty((w.T, w.topk), dtype=torch.int32, device=dev)
+        for _ in range(3):
+            flush.fill_(1.0)
+            nvmla.nvmla_topk_select(sc, w.topk, out=tko)
+        torch.cuda.synchronize()
+        tev = []
+        for k in range(K):
+            if k % GROUP == 0:
+                torch.cuda._sleep(LEAD_CYCLES_PER_STEP * min(GROUP, K - k))
+            flush.fill_(float(k))
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            e[0].record()
+            nvmla.nvmla_topk_select(sc, w.topk, out=tko)
+            e[1].record()
+            tev.append(e)
+        torch.cuda.synchronize()
+        t_us = statistics.mean([e[0].elapsed_time(e[1]) for e in tev]) * 1e3
+        topk_sel = {"us_per_call": t_us, "T": w.T, "candidates": ctx, "topk": w.topk,
+                    "score_bytes": w.T * ctx * 4, "gbs": w.T * ctx * 4 / (t_us * 1e-6) / 1e9}
+        del sc
+
     # ---------------- pack of the write+read workload's 6144-token chunk
     plat, prope, pslots = workloads.pack_chunk(seed=4, n=6144, num_pages=2188)
     pcache = torch.zeros((2188, 64, 352), dtype=torch.uint8, device=dev)
@@ -562,6 +591,7 @@ def main():
                        "frac_hbm": pack_bytes / (pack_us * 1e-6) / 1e9 / bw},
         "staged": staged,
         "layered": layered,
+        "topk_select": topk_sel,
         "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "how": "per step: one host-to-device copy of every input from pinned memory, nvfp4_mla_pack, "
                        "sparse_mla_decode, one device-to-host copy of out and lse, replayed as a CUDA graph; "

@@ -317,6 +317,32 @@ nvmla_status sparse_mla_decode_fp8rows(const void* q_latent, const void* q_rope,
 size_t sparse_mla_decode_fp8rows_workspace_size(int32_t T, int32_t H, int32_t topk,
                                                 const nvmla_decode_options* opts);
 
+/*
+ * nvmla_topk_select -- the step upstream of the decode: each query token's
+ * top-k positions by score as the fixed-length, -1 padded list that
+ * sparse_mla_decode consumes. [4-bit, item 3: 2048-slot lists, empty slots
+ * padded; Serving, "A native NVFP4 sparse-MLA decode kernel": the decode
+ * consumes the positions the sparse indexer selected.] The indexer's scores
+ * need trained weights the pages do not give: they are an input here.
+ *
+ *   scores     (device) fp32 [T][row_stride], 4-byte aligned; token t's
+ *              candidates are positions 0 .. length_t - 1 of row t.
+ *   ncols      columns that hold scores (row_stride >= ncols >= 0).
+ *   lengths    (device, nullable) int32 [T]: length_t, clamped to
+ *              [0, ncols]; NULL means ncols for every token.
+ *   topk       1..2048, the list length.
+ *   topk_idx   (device) int32 [T][topk], written.
+ *
+ * Row t of topk_idx holds the k = min(topk, length_t) positions with the
+ * largest scores, equal scores ranked by lower position, in increasing
+ * order, then -1 up to topk. -0.0 ranks as +0.0; NaN scores are ranked by
+ * their bits (above +inf when positive) and are not meant as input.
+ * T == 0 is a no-op. Returns NVMLA_OK or an error status (nothing launched).
+ */
+nvmla_status nvmla_topk_select(const float* scores, int64_t row_stride, int32_t ncols,
+                               const int32_t* lengths, int32_t T, int32_t topk,
+                               int32_t* topk_idx, nvmla_stream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char* nvmla_status_string(nvmla_status s);
 

@@ -16,6 +16,8 @@ Calls (same names as the C ABI, see include/nvmla.h):
 * ``nvfp4_mla_pack_layered(latent, rope, slot_mapping, cache, layer)`` and
   ``sparse_mla_decode_layered(q_latent, q_rope, cache, layer, block_table, topk_idx, sm_scale, ...)``
   (one layer of a block-major multi-layer cache [num_blocks, num_layers, 64, 352])
+* ``nvmla_topk_select(scores, topk, lengths=None)`` (the -1 padded top-k
+  lists the decode consumes, from given scores)
 * ``nvfp4_stage_dequant_fp8(cache, block_table, topk_idx, ...)`` and
   ``sparse_mla_decode_fp8rows(q_latent, q_rope, fp8_rows, row_idx, sm_scale, ...)``
   (the staged baseline)
@@ -32,7 +34,7 @@ __all__ = [
     "NvmlaError", "nvfp4_mla_pack", "sparse_mla_decode", "sparse_mla_decode_workspace_size", "sparse_mla_decode_fp8rows_workspace_size", "launch_count",
     "nvfp4_stage_dequant_fp8", "sparse_mla_decode_fp8rows", "library_path", "load",
     "sparse_mla_decode_noalloc", "sparse_mla_decode_noalloc_max_scratch",
-    "nvfp4_mla_pack_layered", "sparse_mla_decode_layered",
+    "nvfp4_mla_pack_layered", "sparse_mla_decode_layered", "nvmla_topk_select",
     "IMPL_AUTO", "IMPL_MMA", "IMPL_TCGEN05", "ROW_BYTES", "FP8_ROW_BYTES", "PAGE_TOKENS",
 ]
 
@@ -88,6 +90,7 @@ def load():
         "nvfp4_stage_dequant_fp8": (I32, [P, I64, P, I32, I32, P, I32, P, P, I32, P, P, P, P]),
         "sparse_mla_decode_fp8rows": (I32, [P, P, P, P, I32, I32, I32, F, P, P, P, SZ, P, OPT, P]),
         "sparse_mla_decode_fp8rows_workspace_size": (SZ, [I32, I32, I32, OPT]),
+        "nvmla_topk_select": (I32, [P, I64, I32, P, I32, I32, P, P]),
         "nvmla_status_string": (ctypes.c_char_p, [I32]),
         "nvmla_last_error": (ctypes.c_char_p, []),
         "nvmla_version": (I32, []),
@@ -242,6 +245,31 @@ def sparse_mla_decode_layered(q_latent: torch.Tensor, q_rope: torch.Tensor, cach
                                          float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
                                          _ptr(err_word), opts, _stream(q_latent, stream)))
     return out, lse
+
+
+def nvmla_topk_select(scores: torch.Tensor, topk: int = 2048, lengths: Optional[torch.Tensor] = None,
+                      out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Top-k positions by score per row of scores [T, ncols] (fp32, unit
+    inner stride), the first lengths[t] columns of row t being candidates;
+    returns int32 [T, topk]: chosen positions in increasing order, then -1."""
+    _need(scores, "scores", torch.float32, 2, contiguous=False)
+    if scores.shape[1] > 0 and scores.stride(1) != 1:
+        raise ValueError("scores must have unit inner stride")
+    T, ncols = scores.shape
+    if lengths is not None:
+        _need(lengths, "lengths", torch.int32, 1)
+        if lengths.shape[0] != T:
+            raise ValueError("lengths must be [T]")
+    if out is None:
+        out = torch.empty((T, topk), dtype=torch.int32, device=scores.device)
+    _need(out, "out", torch.int32, 2)
+    if tuple(out.shape) != (T, topk):
+        raise ValueError("out must be [T, topk]")
+    stride = scores.stride(0) if T > 1 else ncols
+    lib = load()
+    _check(lib.nvmla_topk_select(_ptr(scores), max(stride, ncols), ncols, _ptr(lengths), T, int(topk), _ptr(out),
+                                 _stream(scores, stream)))
+    return out
 
 
 def sparse_mla_decode_workspace_size(T: int, H: int, topk: int, impl=None, num_splits=None) -> int:

@@ -22,6 +22,9 @@ cudaError_t launch_decode_mma(int fmt, const void*, const void*, const uint8_t*,
 int mma_default_splits(int T, int H, int topk, int num_sms);
 size_t mma_workspace_bytes(int T, int H, int splits);
 
+cudaError_t launch_topk_select(const float*, int64_t, int32_t, const int32_t*, int32_t, int32_t, int32_t*,
+                               cudaStream_t);
+
 // tcgen05 path (decode_tc.cu)
 bool tc_supported(int H);
 bool tc_fp8_rows_supported(int H);
@@ -336,6 +339,22 @@ nvmla_status sparse_mla_decode(const void* q_latent, const void* q_rope, const u
   return sparse_mla_decode_ex(q_latent, q_rope, cache, num_pages, block_table, num_seqs, max_pages_per_seq, topk_idx,
                               topk, q_seq_idx, seq_lens, T, H, sm_scale, out, lse, workspace, workspace_bytes,
                               err_word, nullptr, stream);
+}
+
+nvmla_status nvmla_topk_select(const float* scores, int64_t row_stride, int32_t ncols, const int32_t* lengths,
+                               int32_t T, int32_t topk, int32_t* topk_idx, nvmla_stream_t stream) {
+  if (T < 0) return fail(NVMLA_ERR_INVALID_ARG, "T = %d must be >= 0", T);
+  if (topk < 1 || topk > NVMLA_MAX_TOPK)
+    return fail(NVMLA_ERR_UNSUPPORTED, "topk = %d must be in [1, %d]", topk, NVMLA_MAX_TOPK);
+  if (ncols < 0) return fail(NVMLA_ERR_INVALID_ARG, "ncols = %d must be >= 0", ncols);
+  if (row_stride < ncols) return fail(NVMLA_ERR_INVALID_ARG, "row_stride must be >= ncols");
+  if (T == 0) return NVMLA_OK;
+  if ((!scores && ncols > 0) || !topk_idx) return fail(NVMLA_ERR_INVALID_ARG, "null scores/topk_idx");
+  if (!aligned(scores, 4) || !aligned(topk_idx, 4) || (lengths && !aligned(lengths, 4)))
+    return fail(NVMLA_ERR_INVALID_ARG, "scores, lengths and topk_idx must be 4-byte aligned");
+  return counted(launch_topk_select(scores, row_stride, ncols, lengths, T, topk, topk_idx,
+                                    reinterpret_cast<cudaStream_t>(stream)),
+                 1, "nvmla_topk_select launch");
 }
 
 nvmla_status nvfp4_stage_dequant_fp8(const uint8_t* cache, int64_t num_pages, const int32_t* block_table,

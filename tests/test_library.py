@@ -132,3 +132,17 @@ def test_layered_calls_reject_bad_layers(lib):
         assert call(cache=P(0x10010)) == 1      # misaligned cache
         assert b"" != L.nvmla_last_error()
     assert dec(T=0) == 0 and pk(n=0) == 0       # no-ops, nothing touched
+
+
+def test_topk_select_rejects_bad_arguments(lib):
+    L = _raw(lib)
+    P = ctypes.c_void_p
+    ok = P(0x10000)
+    assert L.nvmla_topk_select(ok, 100, 100, None, 3, 0, ok, None) == 2        # topk 0
+    assert L.nvmla_topk_select(ok, 100, 100, None, 3, 4096, ok, None) == 2     # topk > 2048
+    assert L.nvmla_topk_select(ok, 50, 100, None, 3, 2048, ok, None) == 1      # stride < ncols
+    assert L.nvmla_topk_select(None, 100, 100, None, 3, 2048, ok, None) == 1
+    assert L.nvmla_topk_select(ok, 100, 100, None, 3, 2048, None, None) == 1
+    assert L.nvmla_topk_select(P(0x10002), 100, 100, None, 3, 2048, ok, None) == 1
+    assert L.nvmla_topk_select(ok, 100, 100, None, -1, 2048, ok, None) == 1
+    assert L.nvmla_topk_select(ok, 100, 100, None, 0, 2048, ok, None) == 0     # no-op
