@@ -51,6 +51,7 @@ def parse():
     ap.add_argument("--no-staged", action="store_true")
     ap.add_argument("--no-layered", action="store_true")
     ap.add_argument("--no-topk", action="store_true")
+    ap.add_argument("--no-fp8", action="store_true")
     return ap.parse_args()
 
 
@@ -502,6 +503,42 @@ def main():
                    "bitwise_equal_to_one_layer_decode": same}
         del lcache
 
+    # ---------------- the same decode over the FP8 cache (576-byte rows of the
+    # same tokens) on the same kernel design, same protocol
+    fp8 = None
+    if not args.no_fp8 and args.kernel != "mma" and w.H % 64 == 0:
+        lat_all, rope_all, slots_all = w.all_written()
+        fcache = torch.zeros((cache.shape[0], 64, 576), dtype=torch.uint8, device=dev)
+        nvmla.fp8_mla_pack(lat_all.to(dev), rope_all.to(dev), slots_all.to(dev), fcache)
+        nvmla.fp8_mla_pack(d_new_lat, d_new_rope, d_new_slots, fcache)
+        fo, fl = torch.empty_like(out), torch.empty_like(lse)
+
+        def fp8_call():
+            nvmla.sparse_mla_decode_fp8cache(ql, qr, fcache, bt, tk, w.sm_scale, out=fo, lse=fl, q_seq_idx=qs,
+                                             seq_lens=sl, workspace=ws)
+
+        for _ in range(3):
+            flush.fill_(1.0)
+            fp8_call()
+        torch.cuda.synchronize()
+        fev = []
+        for k in range(K):
+            if k % GROUP == 0:
+                torch.cuda._sleep(LEAD_CYCLES_PER_STEP * min(GROUP, K - k))
+            flush.fill_(float(k))
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            e[0].record()
+            fp8_call()
+            e[1].record()
+            fev.append(e)
+        torch.cuda.synchronize()
+        f_us = statistics.mean([e[0].elapsed_time(e[1]) for e in fev]) * 1e3
+        f_bytes = alg["bytes"] - alg["valid_slots"] * (352 - 576)
+        fp8 = {"us_per_call": f_us, "row_bytes": 576, "cache_bytes": fcache.numel(),
+               "algorithmic_bytes": f_bytes, "effective_hbm_gbs": f_bytes / (f_us * 1e-6) / 1e9,
+               "nvfp4_cache_bytes": cache.numel()}
+        del fcache
+
     # ---------------- the step upstream: top-2048 lists from scores of the
     # whole context (synthetic N(0,1) scores, seeded), same protocol
     topk_sel = None
@@ -592,6 +629,7 @@ def main():
         "staged": staged,
         "layered": layered,
         "topk_select": topk_sel,
+        "fp8_cache": fp8,
         "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "how": "per step: one host-to-device copy of every input from pinned memory, nvfp4_mla_pack, "
                        "sparse_mla_decode, one device-to-host copy of out and lse, replayed as a CUDA graph; "

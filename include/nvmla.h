@@ -343,6 +343,41 @@ nvmla_status nvmla_topk_select(const float* scores, int64_t row_stride, int32_t 
                                const int32_t* lengths, int32_t T, int32_t topk,
                                int32_t* topk_idx, nvmla_stream_t stream);
 
+/*
+ * The FP8 cache the NVFP4 format is measured against: 576-byte rows
+ * [num_pages][64][576] (32-byte aligned), bytes 0-511 the latent and
+ * 512-575 the RoPE values, each one E4M3 byte (round to nearest even,
+ * saturating at 448, sign of zero kept; no scale). [Serving, "Making room
+ * for low-latency decode": 576 bytes per token for an FP8 row; KV, "KV
+ * cache and data transfer": the FP8 decode at 13.7 us beside 12.0 us for
+ * NVFP4.]
+ *
+ * fp8_mla_pack: arguments, checks and errors as nvfp4_mla_pack, writing
+ * 576-byte rows.
+ * sparse_mla_decode_fp8cache: arguments, results and errors as
+ * sparse_mla_decode_ex over such a cache; it runs on the tcgen05 kernel
+ * only: NVMLA_ERR_UNSUPPORTED unless H is a multiple of 64 (and for
+ * impl = NVMLA_IMPL_MMA). The workspace is sized by
+ * sparse_mla_decode_workspace_size_ex with impl = NVMLA_IMPL_TCGEN05.
+ */
+nvmla_status fp8_mla_pack(const void* latent_bf16, int64_t latent_stride,
+                          const void* rope_bf16, int64_t rope_stride,
+                          const int32_t* slot_mapping, int64_t n_tokens,
+                          uint8_t* cache, int64_t num_pages,
+                          int32_t* err_word, nvmla_stream_t stream);
+
+nvmla_status sparse_mla_decode_fp8cache(const void* q_latent, const void* q_rope,
+                                        const uint8_t* cache, int64_t num_pages,
+                                        const int32_t* block_table, int32_t num_seqs,
+                                        int32_t max_pages_per_seq,
+                                        const int32_t* topk_idx, int32_t topk,
+                                        const int32_t* q_seq_idx, const int32_t* seq_lens,
+                                        int32_t T, int32_t H, float sm_scale,
+                                        void* out, float* lse,
+                                        void* workspace, size_t workspace_bytes,
+                                        int32_t* err_word, const nvmla_decode_options* opts,
+                                        nvmla_stream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char* nvmla_status_string(nvmla_status s);
 

@@ -16,6 +16,9 @@ Calls (same names as the C ABI, see include/nvmla.h):
 * ``nvfp4_mla_pack_layered(latent, rope, slot_mapping, cache, layer)`` and
   ``sparse_mla_decode_layered(q_latent, q_rope, cache, layer, block_table, topk_idx, sm_scale, ...)``
   (one layer of a block-major multi-layer cache [num_blocks, num_layers, 64, 352])
+* ``fp8_mla_pack(latent, rope, slot_mapping, cache)`` and
+  ``sparse_mla_decode_fp8cache(q_latent, q_rope, cache, block_table, topk_idx, sm_scale, ...)``
+  (the 576-byte FP8 cache the NVFP4 format is measured against)
 * ``nvmla_topk_select(scores, topk, lengths=None)`` (the -1 padded top-k
   lists the decode consumes, from given scores)
 * ``nvfp4_stage_dequant_fp8(cache, block_table, topk_idx, ...)`` and
@@ -35,6 +38,7 @@ __all__ = [
     "nvfp4_stage_dequant_fp8", "sparse_mla_decode_fp8rows", "library_path", "load",
     "sparse_mla_decode_noalloc", "sparse_mla_decode_noalloc_max_scratch",
     "nvfp4_mla_pack_layered", "sparse_mla_decode_layered", "nvmla_topk_select",
+    "fp8_mla_pack", "sparse_mla_decode_fp8cache",
     "IMPL_AUTO", "IMPL_MMA", "IMPL_TCGEN05", "ROW_BYTES", "FP8_ROW_BYTES", "PAGE_TOKENS",
 ]
 
@@ -91,6 +95,9 @@ def load():
         "sparse_mla_decode_fp8rows": (I32, [P, P, P, P, I32, I32, I32, F, P, P, P, SZ, P, OPT, P]),
         "sparse_mla_decode_fp8rows_workspace_size": (SZ, [I32, I32, I32, OPT]),
         "nvmla_topk_select": (I32, [P, I64, I32, P, I32, I32, P, P]),
+        "fp8_mla_pack": (I32, [P, I64, P, I64, P, I64, P, I64, P, P]),
+        "sparse_mla_decode_fp8cache": (I32, [P, P, P, I64, P, I32, I32, P, I32, P, P, I32, I32, F, P, P, P, SZ, P, OPT,
+                                             P]),
         "nvmla_status_string": (ctypes.c_char_p, [I32]),
         "nvmla_last_error": (ctypes.c_char_p, []),
         "nvmla_version": (I32, []),
@@ -244,6 +251,77 @@ def sparse_mla_decode_layered(q_latent: torch.Tensor, q_rope: torch.Tensor, cach
                                          _ptr(topk_idx), topk, _ptr(q_seq_idx), _ptr(seq_lens), T, H,
                                          float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
                                          _ptr(err_word), opts, _stream(q_latent, stream)))
+    return out, lse
+
+
+def fp8_mla_pack(latent: torch.Tensor, rope: torch.Tensor, slot_mapping: torch.Tensor, cache: torch.Tensor,
+                 err_word: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Write latent [N,512] / rope [N,64] (bf16) as 576-byte E4M3 rows into
+    cache [num_pages, 64, 576] (uint8) at slot_mapping [N]. Returns cache."""
+    _need(latent, "latent", torch.bfloat16, 2, contiguous=False)
+    _need(rope, "rope", torch.bfloat16, 2, contiguous=False)
+    _need(slot_mapping, "slot_mapping", torch.int32, 1)
+    _need(cache, "cache", torch.uint8, 3)
+    if latent.shape[1] != 512 or rope.shape[1] != 64 or latent.stride(1) != 1 or rope.stride(1) != 1:
+        raise ValueError("latent must be [N, 512] and rope [N, 64] with unit inner stride")
+    n = latent.shape[0]
+    if rope.shape[0] != n or slot_mapping.shape[0] != n:
+        raise ValueError("latent, rope and slot_mapping must have the same number of tokens")
+    if cache.shape[1:] != (PAGE_TOKENS, FP8_ROW_BYTES):
+        raise ValueError("cache must be [num_pages, 64, 576]")
+    if err_word is not None:
+        _need(err_word, "err_word", torch.int32, 1)
+    lib = load()
+    ls = latent.stride(0) if n > 1 else 512
+    rs = rope.stride(0) if n > 1 else 64
+    _check(lib.fp8_mla_pack(_ptr(latent), ls, _ptr(rope), rs, _ptr(slot_mapping), n, _ptr(cache), cache.shape[0],
+                            _ptr(err_word), _stream(cache, stream)))
+    return cache
+
+
+def sparse_mla_decode_fp8cache(q_latent: torch.Tensor, q_rope: torch.Tensor, cache: torch.Tensor,
+                               block_table: torch.Tensor, topk_idx: torch.Tensor, sm_scale: float,
+                               out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                               q_seq_idx: Optional[torch.Tensor] = None, seq_lens: Optional[torch.Tensor] = None,
+                               workspace: Optional[torch.Tensor] = None, err_word: Optional[torch.Tensor] = None,
+                               num_splits=None, stream=None):
+    """Sparse MLA decode over the FP8 cache [num_pages, 64, 576] (tcgen05
+    kernel; H a multiple of 64). Returns (out, lse)."""
+    _need(q_latent, "q_latent", torch.bfloat16, 3)
+    _need(q_rope, "q_rope", torch.bfloat16, 3)
+    _need(cache, "cache", torch.uint8, 3)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(topk_idx, "topk_idx", torch.int32, 2)
+    T, H, dl = q_latent.shape
+    if dl != 512 or tuple(q_rope.shape) != (T, H, 64):
+        raise ValueError("q_latent must be [T, H, 512] and q_rope [T, H, 64]")
+    if topk_idx.shape[0] != T:
+        raise ValueError("topk_idx must be [T, topk]")
+    if cache.shape[1:] != (PAGE_TOKENS, FP8_ROW_BYTES):
+        raise ValueError("cache must be [num_pages, 64, 576]")
+    if q_seq_idx is not None:
+        _need(q_seq_idx, "q_seq_idx", torch.int32, 1)
+    if seq_lens is not None:
+        _need(seq_lens, "seq_lens", torch.int32, 1)
+    if out is None:
+        out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=q_latent.device)
+    if lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=q_latent.device)
+    _need(out, "out", torch.bfloat16, 3)
+    _need(lse, "lse", torch.float32, 2)
+    topk = topk_idx.shape[1]
+    opts = _opts(IMPL_TCGEN05, num_splits)
+    lib = load()
+    if workspace is None:
+        nbytes = int(lib.sparse_mla_decode_workspace_size_ex(T, H, topk, opts))
+        if nbytes:
+            workspace = torch.empty(nbytes, dtype=torch.uint8, device=q_latent.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.sparse_mla_decode_fp8cache(_ptr(q_latent), _ptr(q_rope), _ptr(cache), cache.shape[0],
+                                          _ptr(block_table), block_table.shape[0], block_table.shape[1],
+                                          _ptr(topk_idx), topk, _ptr(q_seq_idx), _ptr(seq_lens), T, H,
+                                          float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
+                                          _ptr(err_word), opts, _stream(q_latent, stream)))
     return out, lse
 
 

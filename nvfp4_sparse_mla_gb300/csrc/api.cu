@@ -22,6 +22,8 @@ cudaError_t launch_decode_mma(int fmt, const void*, const void*, const uint8_t*,
 int mma_default_splits(int T, int H, int topk, int num_sms);
 size_t mma_workspace_bytes(int T, int H, int splits);
 
+cudaError_t launch_fp8_pack(const void*, int64_t, const void*, int64_t, const int32_t*, int64_t, uint8_t*, int64_t,
+                            int32_t*, cudaStream_t);
 cudaError_t launch_topk_select(const float*, int64_t, int32_t, const int32_t*, int32_t, int32_t, int32_t*,
                                cudaStream_t);
 
@@ -339,6 +341,53 @@ nvmla_status sparse_mla_decode(const void* q_latent, const void* q_rope, const u
   return sparse_mla_decode_ex(q_latent, q_rope, cache, num_pages, block_table, num_seqs, max_pages_per_seq, topk_idx,
                               topk, q_seq_idx, seq_lens, T, H, sm_scale, out, lse, workspace, workspace_bytes,
                               err_word, nullptr, stream);
+}
+
+nvmla_status fp8_mla_pack(const void* latent_bf16, int64_t latent_stride, const void* rope_bf16, int64_t rope_stride,
+                          const int32_t* slot_mapping, int64_t n_tokens, uint8_t* cache, int64_t num_pages,
+                          int32_t* err_word, nvmla_stream_t stream) {
+  if (n_tokens < 0) return fail(NVMLA_ERR_INVALID_ARG, "n_tokens = %lld must be >= 0", (long long)n_tokens);
+  if (n_tokens == 0) return NVMLA_OK;
+  if (!latent_bf16 || !rope_bf16 || !slot_mapping || !cache)
+    return fail(NVMLA_ERR_INVALID_ARG, "null latent/rope/slot_mapping/cache");
+  if (!aligned(latent_bf16, 16) || latent_stride < NVMLA_LATENT_DIM || latent_stride % 8 != 0)
+    return fail(NVMLA_ERR_INVALID_ARG, "latent must be 16-byte aligned with a stride >= 512 and a multiple of 8");
+  if (!aligned(rope_bf16, 4) || rope_stride < NVMLA_ROPE_DIM || rope_stride % 2 != 0)
+    return fail(NVMLA_ERR_INVALID_ARG, "rope must be 4-byte aligned with an even stride >= 64");
+  if (!aligned(slot_mapping, 4)) return fail(NVMLA_ERR_INVALID_ARG, "slot_mapping must be 4-byte aligned");
+  if (!aligned(cache, 32)) return fail(NVMLA_ERR_INVALID_ARG, "cache must be 32-byte aligned");
+  if (num_pages < 1) return fail(NVMLA_ERR_INVALID_ARG, "num_pages = %lld must be >= 1", (long long)num_pages);
+  if (err_word && !aligned(err_word, 4)) return fail(NVMLA_ERR_INVALID_ARG, "err_word must be 4-byte aligned");
+  return counted(launch_fp8_pack(latent_bf16, latent_stride, rope_bf16, rope_stride, slot_mapping, n_tokens, cache,
+                                 num_pages, err_word, reinterpret_cast<cudaStream_t>(stream)),
+                 1, "fp8_mla_pack launch");
+}
+
+nvmla_status sparse_mla_decode_fp8cache(const void* q_latent, const void* q_rope, const uint8_t* cache,
+                                        int64_t num_pages, const int32_t* block_table, int32_t num_seqs,
+                                        int32_t max_pages_per_seq, const int32_t* topk_idx, int32_t topk,
+                                        const int32_t* q_seq_idx, const int32_t* seq_lens, int32_t T, int32_t H,
+                                        float sm_scale, void* out, float* lse, void* workspace,
+                                        size_t workspace_bytes, int32_t* err_word, const nvmla_decode_options* opts,
+                                        nvmla_stream_t stream) {
+  nvmla_status s = check_shape(T, H, topk, sm_scale);
+  if (s != NVMLA_OK || T == 0) return s;
+  if ((s = check_queries(q_latent, q_rope, out, lse)) != NVMLA_OK) return s;
+  if ((s = check_cache(cache, num_pages, block_table, num_seqs, max_pages_per_seq, topk_idx)) != NVMLA_OK) return s;
+  if (err_word && !aligned(err_word, 4)) return fail(NVMLA_ERR_INVALID_ARG, "err_word must be 4-byte aligned");
+  if (opts && (opts->impl < 0 || opts->impl > NVMLA_IMPL_TCGEN05 || opts->num_splits < 0))
+    return fail(NVMLA_ERR_INVALID_ARG, "bad options");
+  if ((opts && opts->impl == NVMLA_IMPL_MMA) || !tc_supported(H))
+    return fail(NVMLA_ERR_UNSUPPORTED, "the FP8-cache decode runs on the tcgen05 kernel: H a multiple of 64 (H = %d)",
+                H);
+  nvmla_decode_options o{NVMLA_IMPL_TCGEN05, opts ? opts->num_splits : 0};
+  int splits = 1;
+  if ((s = pick_splits(NVMLA_IMPL_TCGEN05, &o, T, H, topk, workspace_bytes, workspace, &splits)) != NVMLA_OK) return s;
+  RowSelect sel{topk_idx, block_table, q_seq_idx, seq_lens, num_pages * NVMLA_PAGE_TOKENS, topk, max_pages_per_seq,
+                num_seqs, NVMLA_PAGE_TOKENS};
+  return counted(launch_decode_tc(2, q_latent, q_rope, cache, sel, nullptr, T, H, topk, sm_scale, out, lse, workspace,
+                                  splits, err_word, reinterpret_cast<cudaStream_t>(stream)),
+                 1, "sparse_mla_decode_fp8cache launch");
 }
 
 nvmla_status nvmla_topk_select(const float* scores, int64_t row_stride, int32_t ncols, const int32_t* lengths,

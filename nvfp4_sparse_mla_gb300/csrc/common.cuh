@@ -104,8 +104,9 @@ __device__ __forceinline__ void report_error(int32_t* err_word, int32_t flag, in
 // consecutive blocks lie page_rows rows apart: 64 for a cache that holds one
 // layer, 64 L when each block keeps the rows of L layers together
 // (block-major, layer-next: the layer's own rows then start at layer * 64).
-__host__ __device__ __forceinline__ int64_t cache_row_offset(int64_t s, int32_t page_rows) {
-  return ((s >> 6) * page_rows + (s & 63)) * kRowBytes;
+__host__ __device__ __forceinline__ int64_t cache_row_offset(int64_t s, int32_t page_rows,
+                                                             int row_bytes = kRowBytes) {
+  return ((s >> 6) * page_rows + (s & 63)) * row_bytes;
 }
 
 // Physical cache slot of slot k of query token t, or -1 (padding or a bad

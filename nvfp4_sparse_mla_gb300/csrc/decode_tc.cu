@@ -495,7 +495,13 @@ __device__ __forceinline__ void warp_reduce32(float (&v)[32], int lane) {
   }
 }
 
+// The cache's row format: 352-byte NVFP4 rows, or 576-byte FP8 rows (512
+// latent + 64 RoPE E4M3 values, no scales).
+enum RowFmt { kFmtNvfp4 = 0, kFmtFp8 = 1 };
+
+template <int FMT>
 __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) {
+  constexpr int kRB = FMT == kFmtFp8 ? kFp8RowBytes : kRowBytes;  // bytes per cache row
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -606,21 +612,41 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
 
   // ---- level 3: rows of the first tile (unpack threads, into registers);
   // the later tiles' slots (softmax threads)
-  uint32_t rc[4][8];  // code bytes of latent chunks 4uh + j
-  uint4 rs;           // scale bytes of groups 16uh .. 16uh + 15
+  // NVFP4: code bytes of latent chunks 4uh + j (32 each) and the scale bytes
+  // of groups 16uh .. 16uh + 15. FP8: the E4M3 bytes of latent chunks
+  // 4uh + 0..2 (64 each; chunk 4uh + 3 is loaded with the RoPE bytes).
+  uint32_t rc[4][FMT == kFmtFp8 ? 16 : 8];
+  uint4 rs;           // scale bytes (NVFP4)
   uint32_t rr[16];    // the 64 RoPE bytes (half 0 only)
   int32_t slot0 = -1;
+  auto row_of = [&](int32_t slot) { return p.cache + cache_row_offset(slot, p.sel.page_rows, kRB); };
+  // the part of a row batch A needs
   auto load_codes = [&](int32_t slot, int j) {
-    if (slot >= 0) ldg_nc_v8(p.cache + cache_row_offset(slot, p.sel.page_rows) + 128 * uh + 32 * j, rc[j]);
+    if constexpr (FMT == kFmtFp8) {
+      if (slot >= 0 && j < 3) {
+        ldg_nc_v8(row_of(slot) + 256 * uh + 64 * j, rc[j]);
+        ldg_nc_v8(row_of(slot) + 256 * uh + 64 * j + 32, rc[j] + 8);
+      }
+    } else {
+      if (slot >= 0) ldg_nc_v8(row_of(slot) + 128 * uh + 32 * j, rc[j]);
+    }
   };
   auto load_scale = [&](int32_t slot) {
-    if (slot >= 0) rs = ldg_nc_v4(p.cache + cache_row_offset(slot, p.sel.page_rows) + kScaleOff + 16 * uh);
+    if constexpr (FMT != kFmtFp8)
+      if (slot >= 0) rs = ldg_nc_v4(row_of(slot) + kScaleOff + 16 * uh);
   };
+  // the part batch B needs beyond that
   auto load_rope = [&](int32_t slot) {
-    if (slot >= 0 && uh == 0) {
-      const uint8_t* row = p.cache + cache_row_offset(slot, p.sel.page_rows);
-      ldg_nc_v8(row + kRopeOff, rr);
-      ldg_nc_v8(row + kRopeOff + 32, rr + 8);
+    if (slot < 0) return;
+    const uint8_t* row = row_of(slot);
+    if constexpr (FMT == kFmtFp8) {
+      ldg_nc_v8(row + 256 * uh + 192, rc[3]);
+      ldg_nc_v8(row + 256 * uh + 224, rc[3] + 8);
+    }
+    if (uh == 0) {
+      constexpr int off = FMT == kFmtFp8 ? kLatent : kRopeOff;
+      ldg_nc_v8(row + off, rr);
+      ldg_nc_v8(row + off + 32, rr + 8);
     }
   };
   if (is_unpack) {
@@ -723,7 +749,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
       if (tid == 0 && i < 2) NVMLA_TRACE_POINT(70 + 10 * i);
       tc_fence_after();
 #pragma unroll
-      for (int j = 0; j < 3; ++j) tmem_store_chunk(rc[j], sc[j], valid, krow + 32 * (2 * j + uh));
+      for (int j = 0; j < 3; ++j) {
+        if constexpr (FMT == kFmtFp8) {
+          tmem_store_rope(rc[j], valid, krow + 32 * (2 * j + uh));
+        } else {
+          tmem_store_chunk(rc[j], sc[j], valid, krow + 32 * (2 * j + uh));
+        }
+      }
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc_fence_before();
       warp_arrive(bar(kBarKFullA), lane);
@@ -737,7 +769,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
       if (!ok) break;
       if (tid == 0 && i < 2) NVMLA_TRACE_POINT(72 + 10 * i);
       tc_fence_after();
-      tmem_store_chunk(rc[3], sc[3], valid, krow + 32 * uh);
+      if constexpr (FMT == kFmtFp8) {
+        tmem_store_rope(rc[3], valid, krow + 32 * uh);
+      } else {
+        tmem_store_chunk(rc[3], sc[3], valid, krow + 32 * uh);
+      }
       if (uh == 0) tmem_store_rope(rr, valid, krow + 64);
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc_fence_before();
@@ -860,7 +896,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
     // (requested together with them, they delay them)
     for (int i = 1 + (sj >> 7); i < ntiles; i += 2) {
       const int32_t sl = slots[i * kTile + (sj & 127)];
-      if (sl >= 0) prefetch_l2(p.cache + cache_row_offset(sl, p.sel.page_rows), kRowBytes);
+      if (sl >= 0) prefetch_l2(p.cache + cache_row_offset(sl, p.sel.page_rows, kRB), kRB);
     }
     // S^T is free for the first tile
     warp_arrive(bar(kBarKFullA), lane);
@@ -1237,11 +1273,14 @@ int tc_prepare() {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
   TcDevice& d = g_tc_dev[dev];
   if (d.ready) return dev;
-  cudaError_t e = cudaFuncSetAttribute(tc::decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       tc::kSmemBytes);
-  if (e != cudaSuccess) return -1;
-  const bool non_portable =
-      cudaFuncSetAttribute(tc::decode_tc_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+  // both row formats: the same launch shape and resources
+  bool non_portable = true;
+  for (auto* k : {tc::decode_tc_kernel<tc::kFmtNvfp4>, tc::decode_tc_kernel<tc::kFmtFp8>}) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kSmemBytes);
+    if (e != cudaSuccess) return -1;
+    non_portable = non_portable &&
+                   cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+  }
   for (int s = 1; s <= tc::kMaxCluster; ++s) {
     d.max_active[s] = 0;
     if (s > 8 && !non_portable) continue;
@@ -1257,7 +1296,7 @@ int tc_prepare() {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, tc::decode_tc_kernel, &cfg) == cudaSuccess) d.max_active[s] = n;
+    if (cudaOccupancyMaxActiveClusters(&n, tc::decode_tc_kernel<tc::kFmtNvfp4>, &cfg) == cudaSuccess) d.max_active[s] = n;
   }
   cudaGetLastError();  // a refused cluster size leaves no sticky error
   d.ready = true;
@@ -1303,7 +1342,8 @@ cudaError_t launch_decode_tc(int fmt, const void* q_latent, const void* q_rope, 
                              const RowSelect& sel, const int32_t* row_idx, int T, int H, int topk, float sm_scale,
                              void* out, float* lse, void* workspace, int splits, int32_t* err_word,
                              cudaStream_t stream) {
-  if (fmt != 0) return cudaErrorNotSupported;
+  // fmt: 0 = NVFP4 rows, 2 = FP8 rows in a paged cache
+  if (fmt != 0 && fmt != 2) return cudaErrorNotSupported;
   (void)row_idx;
   if (tc_prepare() < 0) return cudaErrorInvalidDevice;
   if (splits < 1 || splits > tc::kMaxCluster) return cudaErrorInvalidValue;
@@ -1337,7 +1377,8 @@ cudaError_t launch_decode_tc(int fmt, const void* q_latent, const void* q_rope, 
   attr.val.clusterDim.z = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tc::decode_tc_kernel, p);
+  if (fmt == 2) return cudaLaunchKernelEx(&cfg, tc::decode_tc_kernel<tc::kFmtFp8>, p);
+  return cudaLaunchKernelEx(&cfg, tc::decode_tc_kernel<tc::kFmtNvfp4>, p);
 }
 
 }  // namespace nvmla

@@ -95,4 +95,62 @@ cudaError_t launch_pack(const void* latent, int64_t lat_stride, const void* rope
   return cudaGetLastError();
 }
 
+// fp8_mla_pack: the FP8 cache the NVFP4 rows are compared with (576-byte
+// rows: the 512 latent and 64 RoPE values each as one E4M3 byte, nearest
+// even, saturating, no scale; "Prime Inference: Fast, Reliable Serving for
+// Frontier Open Models", section "Making room for low-latency decode": 576
+// bytes per token before the NVFP4 change). One warp per token: lane l owns
+// latent values 16l .. 16l + 15 and RoPE values 2l, 2l + 1; the row is
+// assembled in shared memory and written as 36 aligned 16-byte stores.
+__global__ void __launch_bounds__(kPackWarps * 32)
+fp8_pack_kernel(const __nv_bfloat16* __restrict__ latent, int64_t lat_stride, const __nv_bfloat16* __restrict__ rope,
+                int64_t rope_stride, const int32_t* __restrict__ slot_mapping, int64_t n_tokens,
+                uint8_t* __restrict__ cache, int64_t num_slots, int32_t* err_word) {
+  __shared__ __align__(16) uint8_t rowbuf[kPackWarps][kFp8RowBytes];
+  const int lane = threadIdx.x & 31;
+  const int wib = threadIdx.x >> 5;
+  uint8_t* row = rowbuf[wib];
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kPackWarps;
+  for (int64_t n = static_cast<int64_t>(blockIdx.x) * kPackWarps + wib; n < n_tokens; n += nwarps) {
+    const int64_t slot = __ldg(slot_mapping + n);
+    if (slot < 0) continue;
+    if (slot >= num_slots) {
+      if (lane == 0) report_error(err_word, NVMLA_ERRW_PACK_SLOT, 1);
+      continue;
+    }
+    const uint4* src = reinterpret_cast<const uint4*>(latent + n * lat_stride + lane * 16);
+    const uint4 a = __ldg(src);
+    const uint4 b = __ldg(src + 1);
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t q[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t lo = f32x2_to_e4m3x2(bf16_bits_to_f32(w[2 * i] & 0xffffu), bf16_bits_to_f32(w[2 * i] >> 16));
+      const uint32_t hi =
+          f32x2_to_e4m3x2(bf16_bits_to_f32(w[2 * i + 1] & 0xffffu), bf16_bits_to_f32(w[2 * i + 1] >> 16));
+      q[i] = lo | (hi << 16);
+    }
+    *reinterpret_cast<uint4*>(row + 16 * lane) = make_uint4(q[0], q[1], q[2], q[3]);
+    const uint32_t rw = __ldg(reinterpret_cast<const uint32_t*>(rope + n * rope_stride) + lane);
+    *reinterpret_cast<uint16_t*>(row + kLatent + 2 * lane) =
+        f32x2_to_e4m3x2(bf16_bits_to_f32(rw & 0xffffu), bf16_bits_to_f32(rw >> 16));
+    __syncwarp();
+    uint8_t* dst = cache + slot * kFp8RowBytes;
+    for (int c = lane; c < kFp8RowBytes / 16; c += 32)
+      reinterpret_cast<uint4*>(dst)[c] = reinterpret_cast<const uint4*>(row)[c];
+    __syncwarp();
+  }
+}
+
+cudaError_t launch_fp8_pack(const void* latent, int64_t lat_stride, const void* rope, int64_t rope_stride,
+                            const int32_t* slot_mapping, int64_t n_tokens, uint8_t* cache, int64_t num_pages,
+                            int32_t* err_word, cudaStream_t stream) {
+  const int64_t blocks_needed = (n_tokens + kPackWarps - 1) / kPackWarps;
+  const int blocks = static_cast<int>(blocks_needed < 152 * 16 ? blocks_needed : 152 * 16);
+  fp8_pack_kernel<<<blocks, kPackWarps * 32, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(latent), lat_stride, static_cast<const __nv_bfloat16*>(rope), rope_stride,
+      slot_mapping, n_tokens, cache, num_pages * kPage, err_word);
+  return cudaGetLastError();
+}
+
 }  // namespace nvmla

@@ -27,6 +27,8 @@ Modules:
 * ``attention`` -- masked sparse softmax attention over selected rows (pinned).
 * ``staged``    -- the staged baseline's FP8 requantisation (pinned).
 * ``layered``   -- one layer of a block-major multi-layer cache (pinned).
+* ``fp8cache``  -- the 576-byte FP8 cache and its decode (pinned).
+* ``topk``      -- the -1 padded top-k lists (pinned).
 
 Every function is pinned by tests under ``tests/`` against facts the pages
 or mathematics fix (printed grid and byte counts, library conversions,

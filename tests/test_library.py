@@ -146,3 +146,17 @@ def test_topk_select_rejects_bad_arguments(lib):
     assert L.nvmla_topk_select(P(0x10002), 100, 100, None, 3, 2048, ok, None) == 1
     assert L.nvmla_topk_select(ok, 100, 100, None, -1, 2048, ok, None) == 1
     assert L.nvmla_topk_select(ok, 100, 100, None, 0, 2048, ok, None) == 0     # no-op
+
+
+def test_fp8_cache_calls_reject_bad_arguments(lib):
+    L = _raw(lib)
+    P = ctypes.c_void_p
+    ok = P(0x10000)
+    assert L.fp8_mla_pack(None, 512, ok, 64, ok, 10, ok, 1, None, None) == 1
+    assert L.fp8_mla_pack(ok, 512, ok, 64, ok, 10, P(0x10008), 1, None, None) == 1
+    assert L.fp8_mla_pack(ok, 512, ok, 64, ok, 0, ok, 1, None, None) == 0
+    args = [ok, ok, ok, 10, ok, 1, 4, ok, 2048, None, None, 15, 32, 0.1, ok, ok, None, 0, None, None, None]
+    assert L.sparse_mla_decode_fp8cache(*args) == 2            # H = 32: not on the tcgen05 kernel
+    args[12] = 64
+    args[2] = P(0x10008)
+    assert L.sparse_mla_decode_fp8cache(*args) == 1            # misaligned cache
