@@ -437,10 +437,29 @@ def main():
         ws2 = nvmla.sparse_mla_decode_fp8rows_workspace_size(w.T, w.H, w.topk, impl=impl)
         ws2 = torch.empty(max(ws2, 16), dtype=torch.uint8, device=dev)
 
-        def staged_call():
-            nvmla.nvfp4_stage_dequant_fp8(cache, bt, tk, qs, sl, fp8_rows=buf, row_idx=ridx)
+        # stage 2 on the tcgen05 kernel: the staging buffer read as a paged
+        # FP8 cache, token t's rows being pages t * topk / 64 onwards (one
+        # block-table row per token; the list entries are the row indices)
+        tc_stage2 = args.kernel != "mma" and w.H % 64 == 0 and w.topk % 64 == 0
+        if tc_stage2:
+            ppt = w.topk // 64
+            sbt = torch.arange(w.T * ppt, dtype=torch.int32, device=dev).view(w.T, ppt)
+            sqs = torch.arange(w.T, dtype=torch.int32, device=dev)
+            sview = buf.view(w.T * ppt, 64, 576)
+
+        def attend_tc():
+            nvmla.sparse_mla_decode_fp8cache(ql, qr, sview, sbt, ridx, w.sm_scale, out=out, lse=lse, q_seq_idx=sqs,
+                                             workspace=ws)
+
+        def attend_mma():
             nvmla.sparse_mla_decode_fp8rows(ql, qr, buf, ridx, w.sm_scale, out=out, lse=lse, workspace=ws2,
                                             impl=impl)
+
+        def staged_call():
+            nvmla.nvfp4_stage_dequant_fp8(cache, bt, tk, qs, sl, fp8_rows=buf, row_idx=ridx)
+            attend_mma()
+            if tc_stage2:
+                attend_tc()
 
         for _ in range(3):
             flush.fill_(1.0)
@@ -455,16 +474,38 @@ def main():
             e[0].record()
             nvmla.nvfp4_stage_dequant_fp8(cache, bt, tk, qs, sl, fp8_rows=buf, row_idx=ridx)
             e[1].record()
-            nvmla.sparse_mla_decode_fp8rows(ql, qr, buf, ridx, w.sm_scale, out=out, lse=lse, workspace=ws2,
-                                            impl=impl)
+            attend_mma()
             e[2].record()
             sev.append(e)
         torch.cuda.synchronize()
         s1 = [e[0].elapsed_time(e[1]) for e in sev]
         s2 = [e[1].elapsed_time(e[2]) for e in sev]
-        staged = {"us_per_call": statistics.mean([a + b for a, b in zip(s1, s2)]) * 1e3,
-                  "dequant_us": statistics.mean(s1) * 1e3, "attend_us": statistics.mean(s2) * 1e3,
+        attend_us = statistics.mean(s2) * 1e3
+        how = "stage 2 on the mma.sync kernel (FP8 rows by index)"
+        staged = {"dequant_us": statistics.mean(s1) * 1e3, "attend_mma_us": attend_us,
                   "fp8_buffer_bytes": w.T * w.topk * 576}
+        if tc_stage2:
+            # the tcgen05 stage 2 timed right after an untimed stage 1, as the
+            # mma one is (the buffer partly in L2)
+            tcev = []
+            for k in range(K):
+                if k % GROUP == 0:
+                    torch.cuda._sleep(LEAD_CYCLES_PER_STEP * min(GROUP, K - k))
+                flush.fill_(float(k))
+                nvmla.nvfp4_stage_dequant_fp8(cache, bt, tk, qs, sl, fp8_rows=buf, row_idx=ridx)
+                e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+                e[0].record()
+                attend_tc()
+                e[1].record()
+                tcev.append(e)
+            torch.cuda.synchronize()
+            staged["attend_tcgen05_us"] = statistics.mean([e[0].elapsed_time(e[1]) for e in tcev]) * 1e3
+            attend_us = min(attend_us, staged["attend_tcgen05_us"])
+            how = "stage 2 on the faster of the mma.sync kernel (FP8 rows by index) and the tcgen05 kernel (the " \
+                  "buffer read as a paged FP8 cache)"
+        staged["attend_us"] = attend_us
+        staged["us_per_call"] = staged["dequant_us"] + attend_us
+        staged["how"] = how
 
     # ---------------- the same decode over one layer of a block-major cache
     # of 4 layers (the rows of this workload in layer 2); same protocol
