@@ -37,6 +37,13 @@ def test_heavy_ties(lib, cuda):
     check(lib, cuda, s, 2048)
 
 
+def test_many_equal_keys_per_chunk(lib, cuda):
+    # more equal keys in the chosen bin than a CTA keeps in shared memory
+    check(lib, cuda, np.zeros((2, 200_000)), 2048)
+    rng = np.random.default_rng(26)
+    check(lib, cuda, rng.integers(0, 4, (3, 200_000)).astype(np.float64), 2048)
+
+
 def test_short_and_empty_lists(lib, cuda):
     rng = np.random.default_rng(23)
     s = rng.standard_normal((5, 4000))
