@@ -55,6 +55,17 @@ def parse():
     return ap.parse_args()
 
 
+def max_over_ranks(values, world, device):
+    """The element-wise maximum of `values` (floats) over the job's ranks (a
+    no-op for one rank). Replicas exchange nothing but this and barriers."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -345,10 +356,7 @@ def main():
     pack_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
     dec_us = statistics.mean(dec_ms) * 1e3
     step_mean = statistics.mean(step_ms)
-    if world > 1:
-        t = torch.tensor([dec_us, step_mean], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        dec_us, step_mean = float(t[0]), float(t[1])
+    dec_us, step_mean = max_over_ranks([dec_us, step_mean], world, dev)
 
     # ---------------- end to end through the public API with host buffers
     # Every per-step input (queries, index lists, the new tokens) lives in
