@@ -1313,24 +1313,37 @@ int tc_max_splits() {
   return s;
 }
 
-// Key splits per token: enough CTAs to fill the SMs, at most as many
-// clusters as can be resident at once, then the fewest splits that give the
-// busiest CTA the same number of tiles.
+// Key splits per token. Each candidate split count S is costed as the waves
+// of clusters it needs (the clusters of S CTAs the device holds at once, from
+// the occupancy query) times the time of one wave, modelled from measurements
+// at 64 heads and top-2048 on a GB300: a fixed part (start-up and the split
+// combine) plus a per-tile part for the busiest CTA. The cheapest S wins (the
+// smaller on a tie), then the fewest splits that give the busiest CTA the
+// same number of tiles. Up to one wave of clusters this is the largest S
+// that still fits; beyond it, fewer, longer waves can win.
 int tc_default_splits(int T, int H, int topk, int num_sms) {
+  constexpr double kWaveFixedUs = 19.0;  // per wave: start-up, tail, combine
+  constexpr double kTileUs = 5.0;        // per 128-row tile of the busiest CTA
   const int tiles = (topk + tc::kTile - 1) / tc::kTile;
-  const int clusters = T * (H / tc::kHeads);
-  int s = num_sms / max(1, clusters);
-  if (s < 1) s = 1;
-  if (s > tiles) s = tiles;
-  if (s > tc::kMaxCluster) s = tc::kMaxCluster;
+  const int clusters = max(1, T * (H / tc::kHeads));
   const int dev = tc_prepare();
-  if (dev < 0) {
-    if (s > 8) s = 8;
-  } else {
-    while (s > 1 && g_tc_dev[dev].max_active[s] < clusters) --s;
+  int best = 1;
+  double best_cost = -1.0;
+  for (int s = 1; s <= min(tiles, tc::kMaxCluster); ++s) {
+    // clusters of s CTAs resident at once (no device: the portable sizes,
+    // one CTA per SM)
+    const int resident = dev < 0 ? (s <= 8 ? num_sms / s : 0) : g_tc_dev[dev].max_active[s];
+    if (resident < 1) continue;
+    const int waves = (clusters + resident - 1) / resident;
+    const int per = (tiles + s - 1) / s;
+    const double cost = waves * (kWaveFixedUs + kTileUs * per);
+    if (best_cost < 0.0 || cost < best_cost) {
+      best_cost = cost;
+      best = s;
+    }
   }
-  const int per = (tiles + s - 1) / s;  // tiles of the busiest CTA
-  return (tiles + per - 1) / per;       // fewest splits with that load
+  const int per = (tiles + best - 1) / best;  // tiles of the busiest CTA
+  return (tiles + per - 1) / per;             // fewest splits with that load
 }
 
 size_t tc_workspace_bytes(int T, int H, int splits) {
