@@ -14,14 +14,26 @@
 //
 // One cluster of kTopkCtas CTAs per token, CTA r owning a contiguous chunk of
 // the row. An exact radix select of the k-th largest key over the
-// order-preserving 32-bit image of the scores (11 + 11 + 10 bits): every CTA
-// histograms its chunk (the first pass) or its own keys of the chosen bin
-// (kept in shared memory; the other two passes), and reads the other CTAs'
-// histograms through distributed shared memory, so that every CTA picks the
-// same bin. Each CTA then knows how many of its positions lie above the
-// threshold and how many equal it, learns the counts of the CTAs before it,
-// and writes its chosen positions at their place in the list.
+// order-preserving 32-bit image of the scores:
+//  * first pass, bits 31-21: each CTA histograms its chunk (keeping the keys
+//    in shared memory where they fit) and adds its non-zero bins into rank
+//    0's cluster histogram (remote shared-memory atomics); rank 0 picks the
+//    bin holding the k-th largest key and writes it into every CTA;
+//  * each thread lists the chunk offsets of its keys at or above that bin
+//    (every position that can still be chosen; the chunk is walked again
+//    where a list would overflow);
+//  * the keys of the bin, cluster-wide, usually a few thousand: every CTA
+//    copies its own into a pool in rank 0, which finishes the select on them
+//    alone (bits 20-10, then 9-0) and sends each CTA the threshold and the
+//    counts of chosen positions in the chunks before its own; with more of
+//    them than the pool holds, the last two passes run cluster-wide like the
+//    first and the CTAs exchange their counts;
+//  * each CTA marks its chosen positions in bitmaps of its chunk and writes
+//    them in order at their place in the list (or walks the chunk again in
+//    order where it does not fit in shared memory).
 #include <cooperative_groups.h>
+
+#include <cstddef>
 
 #include "common.cuh"
 
@@ -32,7 +44,6 @@ namespace nvmla {
 constexpr int kTopkThreads = 1024;
 constexpr int kTopkWarps = kTopkThreads / 32;
 constexpr int kTopkCtas = 8;  // CTAs per token (a portable cluster)
-constexpr int kCand = 4096;   // keys of the chosen bin a CTA keeps in shared memory
 
 // order-preserving image of a float: a > b (as reals) iff key(a) > key(b)
 __device__ __forceinline__ uint32_t score_key(float f) {
@@ -69,43 +80,101 @@ __device__ __forceinline__ uint32_t block_incl_scan(uint32_t v, uint32_t* warp_t
   return before + x;
 }
 
-struct TopkShared {
-  uint32_t hist[2048];       // this CTA's counts of the current pass
-  uint32_t cand_key[kCand];  // this CTA's keys of the chosen first-pass bin
-  uint32_t cand_pos[kCand];
-  uint32_t warp_tot[kTopkWarps];
-  uint32_t found[2];  // chosen bin, cluster-wide count above it
-  uint32_t ncand;     // keys of the chosen bin in this CTA
-  uint32_t overflow;  // some CTA of the cluster has more than kCand of them
-  uint32_t counts[2];  // this CTA's positions above / equal to the threshold
-};
+constexpr int kChunkKeys = 32 * 1024;     // a chunk of up to this many keys stays in shared memory
+constexpr int kPool = 8 * 1024;           // keys of the first pass's bin rank 0 collects from the cluster
+constexpr int kList = 8;                  // chunk offsets a thread lists after the first pass
+constexpr int kBmWords = kChunkKeys / 32;  // words of a bitmap of the chunk
+static_assert(kBmWords == kTopkThreads, "one bitmap word per thread");
 
-// The cluster-wide histogram (the sum of `hist` over the cluster's CTAs) and
-// the bin that holds the rank-`need` key from the top, into sh.found. Every
-// thread of every CTA of the cluster calls it, once the histograms are
-// complete cluster-wide.
-__device__ __forceinline__ void pick_bin_cluster(cg::cluster_group& cluster, TopkShared& sh, int nb, uint32_t need) {
-  const int tid = threadIdx.x;
-  // bins from the top: thread i holds bins nb-1-2i and nb-2-2i (nb <= 2048)
-  const int b0 = nb - 1 - 2 * tid, b1 = b0 - 1;
-  uint32_t h0 = 0u, h1 = 0u;
-  for (int r = 0; r < kTopkCtas; ++r) {
-    const uint32_t* rh = cluster.map_shared_rank(sh.hist, r);
-    if (b0 >= 0) h0 += rh[b0];
-    if (b1 >= 0) h1 += rh[b1];
+struct TopkShared {
+  uint32_t hist[2048];     // this CTA's counts of the current pass
+  uint32_t cl_hist[2048];  // rank 0: the cluster's counts of the current pass
+  uint32_t bm_gt[kBmWords];  // chosen positions above / equal to the threshold, by chunk offset
+  uint32_t bm_eq[kBmWords];
+  uint32_t warp_tot[kTopkWarps];
+  uint32_t part[kTopkWarps][2 * kTopkCtas];  // rank 0: per warp, pool keys above / equal by source rank
+  uint32_t found[3];  // written by rank 0: chosen bin, cluster-wide count above it, count in it
+  // written by rank 0 (pool path): threshold key, equal keys taken, and the
+  // chosen positions above / equal to it in the chunks before this one
+  uint32_t res[4];
+  uint32_t lower[kTopkCtas][2];  // counts above / equal written by each lower rank (cluster-wide path)
+  uint32_t seg[kTopkCtas][3];    // rank 0: each rank's pool start and length, and its count above the bin
+  // per thread (column), the chunk offsets of its keys at or above the first
+  // pass's bin
+  uint32_t list[kList][kTopkThreads];
+  uint32_t pool_n;               // rank 0: pool slots handed out
+  uint32_t slot;                 // this CTA's pool slots used
+  uint32_t base;                 // this CTA's pool start
+  alignas(16) uint32_t pool[kPool];
+  alignas(16) uint32_t keys[kChunkKeys];  // the chunk's keys, when they fit
+};
+static_assert(offsetof(TopkShared, keys) % 16 == 0, "chunk keys are read 16 bytes at a time");
+static_assert(sizeof(TopkShared) <= 227 * 1024, "shared memory of one CTA");
+
+// Cluster barrier in two halves; every thread of every CTA of the cluster
+// executes both, in the same order. Arrive releases and wait acquires this
+// thread's shared (local and remote) and global memory accesses at cluster
+// scope.
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
+__device__ __forceinline__ void cluster_barrier() {
+  cluster_arrive();
+  cluster_wait();
+}
+
+// this CTA's non-zero counts of bins [0, nb) into rank 0's cluster histogram
+__device__ __forceinline__ void push_hist(cg::cluster_group& cluster, TopkShared& sh, int nb) {
+  uint32_t* dst = cluster.map_shared_rank(sh.cl_hist, 0);
+  for (int b = threadIdx.x; b < nb; b += kTopkThreads) {
+    const uint32_t v = sh.hist[b];
+    if (v != 0u) atomicAdd(dst + b, v);
   }
+}
+
+// Every thread of one CTA: the bin of `h` (nb <= 2048 bins) that holds the
+// rank-`need` key from the top, the count above it and the count in it, as
+// seen by the one thread that finds it (need must lie in 1 .. sum of h).
+// Returns true on that thread. Each bin is cleared after it is read.
+__device__ __forceinline__ bool pick_bin(TopkShared& sh, uint32_t* h, int nb, uint32_t need, uint32_t& bin,
+                                         uint32_t& above, uint32_t& count) {
+  const int tid = threadIdx.x;
+  // bins from the top: thread i holds bins nb-1-2i and nb-2-2i
+  const int b0 = nb - 1 - 2 * tid, b1 = b0 - 1;
+  const uint32_t h0 = b0 >= 0 ? h[b0] : 0u;
+  const uint32_t h1 = b1 >= 0 ? h[b1] : 0u;
   uint32_t total;
   const uint32_t incl = block_incl_scan(h0 + h1, sh.warp_tot, total);
   const uint32_t above0 = incl - h0 - h1, above1 = above0 + h0;
+  if (b0 >= 0) h[b0] = 0u;
+  if (b1 >= 0) h[b1] = 0u;
   if (b0 >= 0 && need > above0 && need <= above0 + h0) {
-    sh.found[0] = static_cast<uint32_t>(b0);
-    sh.found[1] = above0;
+    bin = static_cast<uint32_t>(b0);
+    above = above0;
+    count = h0;
+    return true;
   }
   if (b1 >= 0 && need > above1 && need <= above1 + h1) {
-    sh.found[0] = static_cast<uint32_t>(b1);
-    sh.found[1] = above1;
+    bin = static_cast<uint32_t>(b1);
+    above = above1;
+    count = h1;
+    return true;
   }
-  __syncthreads();
+  return false;
+}
+
+// Rank 0, every thread, once the cluster histogram is complete: the chosen
+// bin, written into every CTA's `found`; the cluster histogram is cleared
+// for the next pass.
+__device__ __forceinline__ void pick_broadcast(cg::cluster_group& cluster, TopkShared& sh, int nb, uint32_t need) {
+  uint32_t bin, above, count;
+  if (pick_bin(sh, sh.cl_hist, nb, need, bin, above, count)) {
+    for (int r = 0; r < kTopkCtas; ++r) {
+      uint32_t* f = cluster.map_shared_rank(sh.found, r);
+      f[0] = bin;
+      f[1] = above;
+      f[2] = count;
+    }
+  }
 }
 
 __global__ void __cluster_dims__(kTopkCtas, 1, 1) __launch_bounds__(kTopkThreads, 1)
@@ -115,7 +184,7 @@ __global__ void __cluster_dims__(kTopkCtas, 1, 1) __launch_bounds__(kTopkThreads
   TopkShared& sh = *reinterpret_cast<TopkShared*>(topk_smem);
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = static_cast<int>(cluster.block_rank());
-  const int t = blockIdx.y, tid = threadIdx.x;
+  const int t = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const float* s = scores + static_cast<int64_t>(t) * stride;
   int32_t* o = out + static_cast<int64_t>(t) * topk;
   int L = lengths ? __ldg(lengths + t) : ncols;
@@ -132,25 +201,39 @@ __global__ void __cluster_dims__(kTopkCtas, 1, 1) __launch_bounds__(kTopkThreads
   // this CTA's chunk: positions [lo, hi), split at multiples of 4
   const int quads = (L + 3) / 4;
   const int lo = 4 * ((rank * quads) / kTopkCtas), hi = min(L, 4 * (((rank + 1) * quads) / kTopkCtas));
+  const int len = hi - lo;
   // rows that start on a 16-byte boundary are read 4 scores at a time
   const bool vec = (reinterpret_cast<uintptr_t>(s) & 15u) == 0;
-  // apply f(key, position) to every position of the chunk
+  // the chunk's keys are kept in shared memory by the first pass
+  const bool in_smem = len <= kChunkKeys;
+  // apply f(key, chunk offset) to every key of the chunk (any order); from
+  // shared memory after the first pass where the chunk fits
   auto for_chunk = [&](auto&& f) {
-    if (vec) {
-      const float4* s4 = reinterpret_cast<const float4*>(s);
-      const int q_hi = hi / 4;
+    if (in_smem) {
+      const int n4 = len / 4;
+      for (int q = tid; q < n4; q += kTopkThreads) {
+        const uint4 v = reinterpret_cast<const uint4*>(sh.keys)[q];
+        f(v.x, 4 * q);
+        f(v.y, 4 * q + 1);
+        f(v.z, 4 * q + 2);
+        f(v.w, 4 * q + 3);
+      }
+      for (int i = 4 * n4 + tid; i < len; i += kTopkThreads) f(sh.keys[i], i);
+    } else if (vec) {
+      const float4* s4 = reinterpret_cast<const float4*>(s + lo);
+      const int n4 = len / 4;
       constexpr int kU = 4;  // 16-byte loads in flight per thread
-      for (int q0 = lo / 4; q0 < q_hi; q0 += kU * kTopkThreads) {
+      for (int q0 = 0; q0 < n4; q0 += kU * kTopkThreads) {
         float4 v[kU];
 #pragma unroll
         for (int r = 0; r < kU; ++r) {
           const int q = q0 + r * kTopkThreads + tid;
-          if (q < q_hi) v[r] = __ldg(s4 + q);
+          if (q < n4) v[r] = __ldg(s4 + q);
         }
 #pragma unroll
         for (int r = 0; r < kU; ++r) {
           const int q = q0 + r * kTopkThreads + tid;
-          if (q < q_hi) {
+          if (q < n4) {
             f(score_key(v[r].x), 4 * q);
             f(score_key(v[r].y), 4 * q + 1);
             f(score_key(v[r].z), 4 * q + 2);
@@ -158,152 +241,370 @@ __global__ void __cluster_dims__(kTopkCtas, 1, 1) __launch_bounds__(kTopkThreads
           }
         }
       }
-      for (int i = 4 * q_hi + tid; i < hi; i += kTopkThreads) f(score_key(__ldg(s + i)), i);
+      for (int i = 4 * n4 + tid; i < len; i += kTopkThreads) f(score_key(__ldg(s + lo + i)), i);
     } else {
-      for (int i = lo + tid; i < hi; i += kTopkThreads) f(score_key(__ldg(s + i)), i);
+      for (int i = tid; i < len; i += kTopkThreads) f(score_key(__ldg(s + lo + i)), i);
     }
   };
 
   // ---- pass 1: key bits 31-21 over the chunk
-  for (int b = tid; b < 2048; b += kTopkThreads) sh.hist[b] = 0u;
+  for (int b = tid; b < 2048; b += kTopkThreads) {
+    sh.hist[b] = 0u;
+    if (rank == 0) sh.cl_hist[b] = 0u;
+  }
+  for (int w = tid; w < kBmWords; w += kTopkThreads) {
+    sh.bm_gt[w] = 0u;
+    sh.bm_eq[w] = 0u;
+  }
   if (tid == 0) {
-    sh.ncand = 0u;
-    sh.overflow = 0u;
+    sh.pool_n = 0u;
+    sh.slot = 0u;
+    // (rank 0 overwrites it; in range whatever happens)
+    sh.found[0] = sh.found[1] = sh.found[2] = 0u;
   }
   __syncthreads();
-  for_chunk([&](uint32_t u, int) { atomicAdd(&sh.hist[u >> 21], 1u); });
-  cluster.sync();
-  uint32_t need = static_cast<uint32_t>(k);  // rank wanted within the current prefix
-  pick_bin_cluster(cluster, sh, 2048, need);
-  const uint32_t bin1 = sh.found[0];
-  uint32_t prefix = bin1 << 21, mask = 0xffe00000u;
-  need -= sh.found[1];
-  // the chunk's positions in bins above the chosen one are all chosen
-  uint32_t n_above = 0u;
-  for (int b = static_cast<int>(bin1) + 1 + tid; b < 2048; b += kTopkThreads) n_above += sh.hist[b];
+  // rank 0's cleared histogram and pool counter are released here and
+  // acquired before the first remote add: the first pass's loads run in
+  // between
+  cluster_arrive();
   {
-    uint32_t tot;
-    block_incl_scan(n_above, sh.warp_tot, tot);
-    n_above = tot;
-  }
-  if (tid == 0 && sh.hist[bin1] > static_cast<uint32_t>(kCand)) {
-    for (int r = 0; r < kTopkCtas; ++r) atomicExch(cluster.map_shared_rank(&sh.overflow, r), 1u);
-  }
-  cluster.sync();  // every CTA is done with the first histograms; overflow is final
-  const bool keep = sh.overflow == 0u;  // the same in every CTA of the cluster
-  // the chunk's keys of the chosen bin, in shared memory
-  if (keep) {
-    for_chunk([&](uint32_t u, int i) {
-      if ((u & mask) == prefix) {
-        const uint32_t c = atomicAdd(&sh.ncand, 1u);
-        sh.cand_key[c] = u;
-        sh.cand_pos[c] = static_cast<uint32_t>(i);
+    // (for_chunk's global walk, also storing the keys)
+    auto hist1 = [&](uint32_t u, int i) {
+      atomicAdd(&sh.hist[u >> 21], 1u);
+      if (in_smem) sh.keys[i] = u;
+    };
+    if (vec) {
+      const float4* s4 = reinterpret_cast<const float4*>(s + lo);
+      const int n4 = len / 4;
+      constexpr int kU = 4;
+      for (int q0 = 0; q0 < n4; q0 += kU * kTopkThreads) {
+        float4 v[kU];
+#pragma unroll
+        for (int r = 0; r < kU; ++r) {
+          const int q = q0 + r * kTopkThreads + tid;
+          if (q < n4) v[r] = __ldg(s4 + q);
+        }
+#pragma unroll
+        for (int r = 0; r < kU; ++r) {
+          const int q = q0 + r * kTopkThreads + tid;
+          if (q < n4) {
+            const uint4 u = make_uint4(score_key(v[r].x), score_key(v[r].y), score_key(v[r].z), score_key(v[r].w));
+            atomicAdd(&sh.hist[u.x >> 21], 1u);
+            atomicAdd(&sh.hist[u.y >> 21], 1u);
+            atomicAdd(&sh.hist[u.z >> 21], 1u);
+            atomicAdd(&sh.hist[u.w >> 21], 1u);
+            if (in_smem) reinterpret_cast<uint4*>(sh.keys)[q] = u;
+          }
+        }
       }
-    });
+      for (int i = 4 * n4 + tid; i < len; i += kTopkThreads) hist1(score_key(__ldg(s + lo + i)), i);
+    } else {
+      for (int i = tid; i < len; i += kTopkThreads) hist1(score_key(__ldg(s + lo + i)), i);
+    }
   }
   __syncthreads();
-  const int nc = static_cast<int>(sh.ncand);
+  cluster_wait();
+  push_hist(cluster, sh, 2048);
+  cluster_barrier();
+  if (rank == 0) pick_broadcast(cluster, sh, 2048, static_cast<uint32_t>(k));
+  cluster_barrier();
+  const uint32_t bin1 = sh.found[0], cnt1 = sh.found[2];
+  uint32_t need = static_cast<uint32_t>(k) - sh.found[1];  // rank wanted within the bin
+  uint32_t prefix = bin1 << 21, mask = 0xffe00000u;
+  uint32_t base_gt = 0u, base_eq = 0u;
 
-  // ---- passes 2 and 3: bits 20-10, then 9-0, over the chosen bin's keys
-#pragma unroll 1
-  for (int pass = 1; pass < 3; ++pass) {
-    const int sb = pass == 1 ? 10 : 0, nb = pass == 1 ? 2048 : 1024;
-    for (int b = tid; b < nb; b += kTopkThreads) sh.hist[b] = 0u;
-    __syncthreads();
-    auto count = [&](uint32_t u, int) {
-      if ((u & mask) == prefix) atomicAdd(&sh.hist[(u >> sb) & (nb - 1)], 1u);
+  // ---- each thread lists its keys at or above the bin (every position
+  // that can still be chosen): short lists, or the chunk is walked instead
+  const uint32_t key_lo = bin1 << 21;
+  uint32_t nl = 0u, nb1 = 0u;  // keys this thread found at or above the bin, and in it
+  if (in_smem) {
+    auto note = [&](uint32_t u, int off) {
+      if (u >= key_lo) {
+        if (nl < static_cast<uint32_t>(kList)) sh.list[nl][tid] = static_cast<uint32_t>(off);
+        ++nl;
+        nb1 += (u >> 21) == bin1 ? 1u : 0u;
+      }
     };
-    if (keep) {
-      for (int c = tid; c < nc; c += kTopkThreads) count(sh.cand_key[c], 0);
-    } else {
-      for_chunk(count);
+    const int n4 = len / 4;
+    for (int q = tid; q < n4; q += kTopkThreads) {
+      const uint4 v = reinterpret_cast<const uint4*>(sh.keys)[q];
+      note(v.x, 4 * q);
+      note(v.y, 4 * q + 1);
+      note(v.z, 4 * q + 2);
+      note(v.w, 4 * q + 3);
     }
-    cluster.sync();
-    pick_bin_cluster(cluster, sh, nb, need);
-    prefix |= sh.found[0] << sb;
-    mask |= static_cast<uint32_t>(nb - 1) << sb;
-    need -= sh.found[1];
-    cluster.sync();  // every CTA is done reading the others' histograms
+    for (int i = 4 * n4 + tid; i < len; i += kTopkThreads) note(sh.keys[i], i);
   }
-  // prefix is the k-th largest key; `need` (>= 1) positions equal to it are
-  // taken, the lowest first
+  const bool listed = in_smem && !__syncthreads_or(nl > static_cast<uint32_t>(kList));
 
-  // ---- this CTA's positions above / equal to the threshold, then the
-  // counts of the CTAs before it
-  uint32_t n_gt = 0u, n_eq = 0u;
-  if (keep) {
-    for (int c = tid; c < nc; c += kTopkThreads) {
-      n_gt += sh.cand_key[c] > prefix ? 1u : 0u;
-      n_eq += sh.cand_key[c] == prefix ? 1u : 0u;
+  if (cnt1 <= static_cast<uint32_t>(kPool)) {
+    // ---- the bin's keys into rank 0's pool (the same decision in every CTA)
+    uint32_t a = 0u;
+    for (int b = static_cast<int>(bin1) + 1 + tid; b < 2048; b += kTopkThreads) a += sh.hist[b];
+    uint32_t above;
+    block_incl_scan(a, sh.warp_tot, above);
+    const uint32_t mine = sh.hist[bin1];
+    if (tid == 0) {
+      const uint32_t b = atomicAdd(cluster.map_shared_rank(&sh.pool_n, 0), mine);
+      sh.base = b;
+      uint32_t* sg = cluster.map_shared_rank(&sh.seg[0][0], 0) + 3 * rank;
+      sg[0] = b;
+      sg[1] = mine;
+      sg[2] = above;
     }
+    __syncthreads();
+    uint32_t* pool0 = cluster.map_shared_rank(sh.pool, 0) + sh.base;
+    if (listed) {
+      uint32_t tot;
+      uint32_t at = block_incl_scan(nb1, sh.warp_tot, tot) - nb1;
+      for (uint32_t j = 0; j < nl; ++j) {
+        const uint32_t u = sh.keys[sh.list[j][tid]];
+        if ((u >> 21) == bin1) {
+          if (at < mine) pool0[at] = u;  // exactly `mine` of them
+          ++at;
+        }
+      }
+    }
+    // otherwise a warp-uniform walk over the chunk's quads, slots taken a
+    // warp at a time
+    const int nq = listed ? 0 : (len + 3) / 4;
+    for (int q0 = 32 * warp; q0 < nq; q0 += kTopkThreads) {
+      const int q = q0 + lane, off = 4 * q;
+      uint32_t key[4] = {0u, 0u, 0u, 0u};
+      if (q < nq) {
+        if (in_smem && off + 4 <= len) {
+          const uint4 v = reinterpret_cast<const uint4*>(sh.keys)[q];
+          key[0] = v.x;
+          key[1] = v.y;
+          key[2] = v.z;
+          key[3] = v.w;
+        } else if (!in_smem && vec && off + 4 <= len) {
+          const float4 v = __ldg(reinterpret_cast<const float4*>(s + lo + off));
+          key[0] = score_key(v.x);
+          key[1] = score_key(v.y);
+          key[2] = score_key(v.z);
+          key[3] = score_key(v.w);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (off + e < len) key[e] = in_smem ? sh.keys[off + e] : score_key(__ldg(s + lo + off + e));
+        }
+      }
+      uint32_t m = 0u;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) m |= (q < nq && off + e < len && (key[e] >> 21) == bin1 ? 1u : 0u) << e;
+      if (__any_sync(0xffffffffu, m != 0u)) {
+        // this lane's slot among the warp's keys of the bin, in lane order
+        const uint32_t c = static_cast<uint32_t>(__popc(m));
+        const uint32_t c0 = __ballot_sync(0xffffffffu, c & 1u), c1 = __ballot_sync(0xffffffffu, c & 2u),
+                       c2 = __ballot_sync(0xffffffffu, c & 4u);
+        const uint32_t below = (1u << lane) - 1u;
+        const uint32_t pre = __popc(c0 & below) + 2u * __popc(c1 & below) + 4u * __popc(c2 & below);
+        const uint32_t tot = __popc(c0) + 2u * __popc(c1) + 4u * __popc(c2);
+        uint32_t at = 0u;
+        if (lane == 0) at = atomicAdd(&sh.slot, tot);
+        at = __shfl_sync(0xffffffffu, at, 0) + pre;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if ((m >> e) & 1u) {
+            if (at < mine) pool0[at] = key[e];  // exactly `mine` of them
+            ++at;
+          }
+        }
+      }
+    }
+    cluster_barrier();
+    if (rank == 0) {
+      // ---- the select within the pool (bits 20-10, then 9-0), then each
+      // rank's counts of chosen positions
+      const int np = static_cast<int>(cnt1);
+#pragma unroll 1
+      for (int pass = 1; pass < 3; ++pass) {
+        const int sb = pass == 1 ? 10 : 0, nb = pass == 1 ? 2048 : 1024;
+        for (int b = tid; b < nb; b += kTopkThreads) sh.hist[b] = 0u;
+        __syncthreads();
+        for (int i = tid; i < np; i += kTopkThreads) {
+          const uint32_t u = sh.pool[i];
+          if ((u & mask) == prefix) atomicAdd(&sh.hist[(u >> sb) & (nb - 1)], 1u);
+        }
+        __syncthreads();
+        uint32_t bin, ab, cnt;
+        if (pick_bin(sh, sh.hist, nb, need, bin, ab, cnt)) {
+          sh.found[0] = bin;
+          sh.found[1] = ab;
+        }
+        __syncthreads();
+        prefix |= sh.found[0] << sb;
+        mask |= static_cast<uint32_t>(nb - 1) << sb;
+        need -= sh.found[1];
+        __syncthreads();  // found is rewritten by the next pass
+      }
+      // pool keys above / equal to the threshold, by the rank they came from
+      uint32_t gt[kTopkCtas], eq[kTopkCtas];
+#pragma unroll
+      for (int r = 0; r < kTopkCtas; ++r) gt[r] = eq[r] = 0u;
+      for (int i = tid; i < np; i += kTopkThreads) {
+        const uint32_t u = sh.pool[i];
+        const uint32_t g = u > prefix ? 1u : 0u, e = u == prefix ? 1u : 0u;
+#pragma unroll
+        for (int r = 0; r < kTopkCtas; ++r) {
+          const bool from = static_cast<uint32_t>(i) - sh.seg[r][0] < sh.seg[r][1];
+          gt[r] += from ? g : 0u;
+          eq[r] += from ? e : 0u;
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < kTopkCtas; ++r) {
+        const uint32_t wg = __reduce_add_sync(0xffffffffu, gt[r]), we = __reduce_add_sync(0xffffffffu, eq[r]);
+        if (lane == 0) {
+          sh.part[warp][2 * r] = wg;
+          sh.part[warp][2 * r + 1] = we;
+        }
+      }
+      __syncthreads();
+      if (tid < 2 * kTopkCtas) {
+        uint32_t v = 0u;
+        for (int w = 0; w < kTopkWarps; ++w) v += sh.part[w][tid];
+        sh.warp_tot[tid] = v;  // [2r]: above, [2r + 1]: equal, from rank r's pool keys
+      }
+      __syncthreads();
+      if (tid < kTopkCtas) {
+        uint32_t bg = 0u, be = 0u;
+        for (int r = 0; r < tid; ++r) {
+          bg += sh.seg[r][2] + sh.warp_tot[2 * r];
+          be += sh.warp_tot[2 * r + 1];
+        }
+        uint32_t* d = cluster.map_shared_rank(sh.res, tid);
+        d[0] = prefix;
+        d[1] = need;
+        d[2] = bg;
+        d[3] = be;
+      }
+    }
+    cluster_barrier();  // the last: no CTA touches another's shared memory after it
+    prefix = sh.res[0];
+    need = sh.res[1];
+    base_gt = sh.res[2];
+    base_eq = sh.res[3];
   } else {
+    // ---- passes 2 and 3 cluster-wide: bits 20-10, then 9-0, of the bin's keys
+#pragma unroll 1
+    for (int pass = 1; pass < 3; ++pass) {
+      const int sb = pass == 1 ? 10 : 0, nb = pass == 1 ? 2048 : 1024;
+      for (int b = tid; b < nb; b += kTopkThreads) sh.hist[b] = 0u;
+      __syncthreads();
+      for_chunk([&](uint32_t u, int) {
+        if ((u & mask) == prefix) atomicAdd(&sh.hist[(u >> sb) & (nb - 1)], 1u);
+      });
+      __syncthreads();
+      push_hist(cluster, sh, nb);
+      cluster_barrier();
+      if (rank == 0) pick_broadcast(cluster, sh, nb, need);
+      cluster_barrier();
+      prefix |= sh.found[0] << sb;
+      mask |= static_cast<uint32_t>(nb - 1) << sb;
+      need -= sh.found[1];
+    }
+    // this CTA's positions above / equal to the threshold, into every higher
+    // rank; then the counts of the ranks below this one
+    uint32_t n_gt = 0u, n_eq = 0u;
     for_chunk([&](uint32_t u, int) {
       n_gt += u > prefix ? 1u : 0u;
       n_eq += u == prefix ? 1u : 0u;
     });
-  }
-  {
     uint32_t tg, te;
     block_incl_scan(n_gt, sh.warp_tot, tg);
     block_incl_scan(n_eq, sh.warp_tot, te);
-    // (with the chosen bin's keys kept, the bins above it hold the rest of
-    // the chunk's keys above the threshold)
-    if (tid == 0) {
-      sh.counts[0] = tg + (keep ? n_above : 0u);
-      sh.counts[1] = te;
+    if (tid > rank && tid < kTopkCtas) {
+      uint32_t* d = cluster.map_shared_rank(&sh.lower[0][0], tid);
+      d[2 * rank] = tg;
+      d[2 * rank + 1] = te;
+    }
+    cluster_barrier();  // the last: no CTA touches another's shared memory after it
+    for (int r = 0; r < rank; ++r) {
+      base_gt += sh.lower[r][0];
+      base_eq += sh.lower[r][1];
     }
   }
-  cluster.sync();
-  uint32_t base_gt = 0u, base_eq = 0u;
-  for (int r = 0; r < rank; ++r) {
-    const uint32_t* rc = cluster.map_shared_rank(sh.counts, r);
-    base_gt += rc[0];
-    base_eq += rc[1];
-  }
-  cluster.sync();  // no CTA leaves while another reads its counts
+  // prefix is the k-th largest key; `need` (>= 1) positions equal to it are
+  // taken cluster-wide, the lowest first; base_gt / base_eq count the chosen
+  // positions above / equal to it in the chunks before this one
 
-  // ---- ordered collection over the chunk: 16 consecutive positions per
-  // thread per round
-  constexpr int kPer = 16;
-#pragma unroll 1
-  for (int start = lo; start < hi; start += kPer * kTopkThreads) {
-    const int p0 = start + kPer * tid;
-    uint32_t key[kPer];
-    if (vec && p0 + kPer <= hi) {
-#pragma unroll
-      for (int q = 0; q < kPer / 4; ++q) {
-        const float4 v = __ldg(reinterpret_cast<const float4*>(s + p0) + q);
-        key[4 * q] = score_key(v.x);
-        key[4 * q + 1] = score_key(v.y);
-        key[4 * q + 2] = score_key(v.z);
-        key[4 * q + 3] = score_key(v.w);
+  if (in_smem) {
+    // ---- ordered collection from bitmaps of the chunk: thread i holds
+    // chunk offsets 32i .. 32i + 31
+    auto mark = [&](uint32_t u, uint32_t off) {
+      if (u > prefix) atomicOr(&sh.bm_gt[off >> 5], 1u << (off & 31));
+      if (u == prefix) atomicOr(&sh.bm_eq[off >> 5], 1u << (off & 31));
+    };
+    if (listed) {
+      for (uint32_t j = 0; j < nl; ++j) {
+        const uint32_t off = sh.list[j][tid];
+        mark(sh.keys[off], off);
       }
     } else {
-#pragma unroll
-      for (int j = 0; j < kPer; ++j) key[j] = p0 + j < hi ? score_key(__ldg(s + p0 + j)) : 0u;
+      for_chunk([&](uint32_t u, int off) { mark(u, static_cast<uint32_t>(off)); });
     }
-    uint32_t gt = 0u, eq = 0u;  // bit j: position p0 + j
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-      if (p0 + j < hi) {
-        gt |= (key[j] > prefix ? 1u : 0u) << j;
-        eq |= (key[j] == prefix ? 1u : 0u) << j;
-      }
-    }
-    const uint32_t c = __popc(gt) | (__popc(eq) << 16);
+    __syncthreads();
+    const uint32_t gw = sh.bm_gt[tid], ew = sh.bm_eq[tid];
+    const uint32_t c = __popc(gw) | (__popc(ew) << 16);
     uint32_t total;
     const uint32_t excl = block_incl_scan(c, sh.warp_tot, total) - c;
     const uint32_t g = base_gt + (excl & 0xffffu), e = base_eq + (excl >> 16);
-    uint32_t sel = gt | eq;
+    uint32_t sel = gw | ew;
     while (sel) {
       const int j = __ffs(sel) - 1;
       sel &= sel - 1u;
       const uint32_t below = (1u << j) - 1u;
-      const uint32_t gj = g + __popc(gt & below), ej = e + __popc(eq & below);
-      if (((gt >> j) & 1u) || ej < need) o[gj + min(ej, need)] = p0 + j;
+      const uint32_t gj = g + __popc(gw & below), ej = e + __popc(ew & below);
+      const uint32_t at = gj + min(ej, need);  // < k when the counts are right; checked all the same
+      if ((((gw >> j) & 1u) || ej < need) && at < static_cast<uint32_t>(k)) o[at] = lo + 32 * tid + j;
     }
-    base_gt += total & 0xffffu;
-    base_eq += total >> 16;
+  } else {
+    // ---- ordered collection over the chunk: 16 consecutive positions per
+    // thread per round
+    constexpr int kPer = 16;
+#pragma unroll 1
+    for (int start = lo; start < hi; start += kPer * kTopkThreads) {
+      const int p0 = start + kPer * tid;
+      uint32_t key[kPer];
+      if (vec && p0 + kPer <= hi) {
+#pragma unroll
+        for (int q = 0; q < kPer / 4; ++q) {
+          const float4 v = __ldg(reinterpret_cast<const float4*>(s + p0) + q);
+          key[4 * q] = score_key(v.x);
+          key[4 * q + 1] = score_key(v.y);
+          key[4 * q + 2] = score_key(v.z);
+          key[4 * q + 3] = score_key(v.w);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) key[j] = p0 + j < hi ? score_key(__ldg(s + p0 + j)) : 0u;
+      }
+      uint32_t gt = 0u, eq = 0u;  // bit j: position p0 + j
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        if (p0 + j < hi) {
+          gt |= (key[j] > prefix ? 1u : 0u) << j;
+          eq |= (key[j] == prefix ? 1u : 0u) << j;
+        }
+      }
+      const uint32_t c = __popc(gt) | (__popc(eq) << 16);
+      uint32_t total;
+      const uint32_t excl = block_incl_scan(c, sh.warp_tot, total) - c;
+      const uint32_t g = base_gt + (excl & 0xffffu), e = base_eq + (excl >> 16);
+      uint32_t sel = gt | eq;
+      while (sel) {
+        const int j = __ffs(sel) - 1;
+        sel &= sel - 1u;
+        const uint32_t below = (1u << j) - 1u;
+        const uint32_t gj = g + __popc(gt & below), ej = e + __popc(eq & below);
+        const uint32_t at = gj + min(ej, need);
+        if ((((gt >> j) & 1u) || ej < need) && at < static_cast<uint32_t>(k)) o[at] = p0 + j;
+      }
+      base_gt += total & 0xffffu;
+      base_eq += total >> 16;
+    }
   }
   if (rank == kTopkCtas - 1)
     for (int i = k + tid; i < topk; i += kTopkThreads) o[i] = -1;

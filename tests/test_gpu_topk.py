@@ -27,6 +27,16 @@ def test_decode_point_size(lib, cuda):
     check(lib, cuda, rng.standard_normal((15, 200_000)), 2048)
 
 
+def test_rows_longer_than_shared_memory_holds(lib, cuda):
+    # 8 chunks of more than 32K keys: every pass reads the chunk from global
+    # memory; one row also has its winners bunched
+    rng = np.random.default_rng(29)
+    s = rng.standard_normal((2, 320_003))
+    s[1, 300_000:302_048] = 5.0
+    check(lib, cuda, s, 2048)
+    check(lib, cuda, s, 2048, lengths=[262_144, 262_148])
+
+
 def test_heavy_ties(lib, cuda):
     rng = np.random.default_rng(22)
     check(lib, cuda, rng.integers(0, 5, (6, 50_000)).astype(np.float64), 2048)
@@ -42,6 +52,38 @@ def test_many_equal_keys_per_chunk(lib, cuda):
     check(lib, cuda, np.zeros((2, 200_000)), 2048)
     rng = np.random.default_rng(26)
     check(lib, cuda, rng.integers(0, 4, (3, 200_000)).astype(np.float64), 2048)
+
+
+def test_winners_bunched_in_one_segment(lib, cuda):
+    # the whole list in the last or first few warp segments of one CTA's
+    # chunk (more kept keys than a warp holds: that CTA re-reads its chunk),
+    # and 200 winners inside one segment (they fit)
+    n = 200_000
+    up = np.arange(n, dtype=np.float64)
+    check(lib, cuda, np.stack([up, up[::-1].copy()]), 2048)
+    rng = np.random.default_rng(27)
+    s = rng.standard_normal((2, n))
+    s[0, 51_000:51_200] = 10.0 + rng.random(200)
+    s[1, 120_000:120_200] = 10.0
+    check(lib, cuda, s, 2048)
+
+
+def test_one_thread_with_many_candidates(lib, cuda):
+    # spikes every 4096 positions land on one thread of every CTA, more of
+    # them than the thread lists: the chunk is walked again for them
+    rng = np.random.default_rng(30)
+    s = rng.standard_normal((2, 200_000))
+    for r in range(2):
+        idx = np.arange(200_000)
+        s[r, (idx + 1000 * r) % 4096 < 4] = 100.0 + rng.random(int(((idx + 1000 * r) % 4096 < 4).sum()))
+    check(lib, cuda, s, 2048)
+
+
+def test_rows_not_16_byte_aligned(lib, cuda):
+    rng = np.random.default_rng(28)
+    s = rng.standard_normal((4, 40_001))
+    check(lib, cuda, s, 2048)
+    check(lib, cuda, s, 2048, lengths=[40_001, 40_000, 39_999, 2050])
 
 
 def test_short_and_empty_lists(lib, cuda):
