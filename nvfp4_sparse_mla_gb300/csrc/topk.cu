@@ -102,6 +102,8 @@ struct TopkShared {
   // per thread (column), the chunk offsets of its keys at or above the first
   // pass's bin
   uint32_t list[kList][kTopkThreads];
+  uint32_t few[32];              // rank 0: the last few keys of the select
+  uint32_t nfew;
   uint32_t pool_n;               // rank 0: pool slots handed out
   uint32_t slot;                 // this CTA's pool slots used
   uint32_t base;                 // this CTA's pool start
@@ -259,6 +261,7 @@ __global__ void __cluster_dims__(kTopkCtas, 1, 1) __launch_bounds__(kTopkThreads
   if (tid == 0) {
     sh.pool_n = 0u;
     sh.slot = 0u;
+    sh.nfew = 0u;
     // (rank 0 overwrites it; in range whatever happens)
     sh.found[0] = sh.found[1] = sh.found[2] = 0u;
   }
@@ -313,6 +316,24 @@ __global__ void __cluster_dims__(kTopkCtas, 1, 1) __launch_bounds__(kTopkThreads
   uint32_t prefix = bin1 << 21, mask = 0xffe00000u;
   uint32_t base_gt = 0u, base_eq = 0u;
 
+  const bool pooled = cnt1 <= static_cast<uint32_t>(kPool);  // the same in every CTA
+  const uint32_t mine = sh.hist[bin1];                          // this CTA's keys of the bin
+  if (pooled && warp == 0) {
+    // this CTA's pool segment (one remote atomic, its latency under the
+    // listing below) and its count of keys above the bin
+    uint32_t a = 0u;
+    for (int b = static_cast<int>(bin1) + 1 + lane; b < 2048; b += 32) a += sh.hist[b];
+    a = __reduce_add_sync(0xffffffffu, a);
+    if (lane == 0) {
+      const uint32_t b = atomicAdd(cluster.map_shared_rank(&sh.pool_n, 0), mine);
+      sh.base = b;
+      uint32_t* sg = cluster.map_shared_rank(&sh.seg[0][0], 0) + 3 * rank;
+      sg[0] = b;
+      sg[1] = mine;
+      sg[2] = a;
+    }
+  }
+
   // ---- each thread lists its keys at or above the bin (every position
   // that can still be chosen): short lists, or the chunk is walked instead
   const uint32_t key_lo = bin1 << 21;
@@ -335,28 +356,19 @@ __global__ void __cluster_dims__(kTopkCtas, 1, 1) __launch_bounds__(kTopkThreads
     }
     for (int i = 4 * n4 + tid; i < len; i += kTopkThreads) note(sh.keys[i], i);
   }
-  const bool listed = in_smem && !__syncthreads_or(nl > static_cast<uint32_t>(kList));
+  // one block scan: this thread's first slot among the CTA's keys of the
+  // bin (low half; the CTA has fewer than 2^16 keys when it lists them) and
+  // the number of lists that overflowed (high half)
+  uint32_t scan_tot;
+  const uint32_t packed = (nb1 & 0xffffu) | (nl > static_cast<uint32_t>(kList) ? 0x10000u : 0u);
+  const uint32_t scan_excl = block_incl_scan(packed, sh.warp_tot, scan_tot) - packed;
+  const bool listed = in_smem && (scan_tot >> 16) == 0u;
 
-  if (cnt1 <= static_cast<uint32_t>(kPool)) {
-    // ---- the bin's keys into rank 0's pool (the same decision in every CTA)
-    uint32_t a = 0u;
-    for (int b = static_cast<int>(bin1) + 1 + tid; b < 2048; b += kTopkThreads) a += sh.hist[b];
-    uint32_t above;
-    block_incl_scan(a, sh.warp_tot, above);
-    const uint32_t mine = sh.hist[bin1];
-    if (tid == 0) {
-      const uint32_t b = atomicAdd(cluster.map_shared_rank(&sh.pool_n, 0), mine);
-      sh.base = b;
-      uint32_t* sg = cluster.map_shared_rank(&sh.seg[0][0], 0) + 3 * rank;
-      sg[0] = b;
-      sg[1] = mine;
-      sg[2] = above;
-    }
-    __syncthreads();
+  if (pooled) {
+    // ---- the bin's keys into rank 0's pool
     uint32_t* pool0 = cluster.map_shared_rank(sh.pool, 0) + sh.base;
     if (listed) {
-      uint32_t tot;
-      uint32_t at = block_incl_scan(nb1, sh.warp_tot, tot) - nb1;
+      uint32_t at = scan_excl & 0xffffu;
       for (uint32_t j = 0; j < nl; ++j) {
         const uint32_t u = sh.keys[sh.list[j][tid]];
         if ((u >> 21) == bin1) {
@@ -421,6 +433,38 @@ __global__ void __cluster_dims__(kTopkCtas, 1, 1) __launch_bounds__(kTopkThreads
 #pragma unroll 1
       for (int pass = 1; pass < 3; ++pass) {
         const int sb = pass == 1 ? 10 : 0, nb = pass == 1 ? 2048 : 1024;
+        if (pass == 2 && sh.found[2] <= 32u) {
+          // at most 32 keys share the top 22 bits: their ranks, counted by
+          // one warp, give the threshold
+          for (int i = tid; i < np; i += kTopkThreads) {
+            const uint32_t u = sh.pool[i];
+            if ((u & mask) == prefix) {
+              const uint32_t c = atomicAdd(&sh.nfew, 1u);
+              if (c < 32u) sh.few[c] = u;
+            }
+          }
+          __syncthreads();
+          if (warp == 0) {
+            const uint32_t nf = min(sh.nfew, 32u);
+            const uint32_t u = static_cast<uint32_t>(lane) < nf ? sh.few[lane] : 0u;
+            uint32_t n_gt = 0u, n_ge = 0u;
+            for (uint32_t j = 0; j < nf; ++j) {
+              const uint32_t v = sh.few[j];
+              n_gt += v > u ? 1u : 0u;
+              n_ge += v >= u ? 1u : 0u;
+            }
+            // (lanes holding equal keys write the same values)
+            if (static_cast<uint32_t>(lane) < nf && n_gt < need && need <= n_ge) {
+              sh.found[0] = u;
+              sh.found[1] = n_gt;
+            }
+          }
+          __syncthreads();
+          prefix = sh.found[0];
+          mask = 0xffffffffu;
+          need -= sh.found[1];
+          break;
+        }
         for (int b = tid; b < nb; b += kTopkThreads) sh.hist[b] = 0u;
         __syncthreads();
         for (int i = tid; i < np; i += kTopkThreads) {
@@ -432,6 +476,7 @@ __global__ void __cluster_dims__(kTopkCtas, 1, 1) __launch_bounds__(kTopkThreads
         if (pick_bin(sh, sh.hist, nb, need, bin, ab, cnt)) {
           sh.found[0] = bin;
           sh.found[1] = ab;
+          sh.found[2] = cnt;
         }
         __syncthreads();
         prefix |= sh.found[0] << sb;
