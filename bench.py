@@ -678,7 +678,7 @@ def main():
                        "frac_hbm": pack_bytes / (pack_us * 1e-6) / 1e9 / bw},
         "staged": staged,
         "layered": layered,
-        "topk_select": topk_sel,
+        "topk_select": (dict(topk_sel, frac_hbm=topk_sel["gbs"] / bw) if topk_sel else None),
         "fp8_cache": fp8,
         "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "how": "per step: one host-to-device copy of every input from pinned memory, nvfp4_mla_pack, "
