@@ -106,6 +106,32 @@ def test_workspace_size_is_host_only(lib):
     assert n == 15 * 8 * 64 * 514 * 4
 
 
+@pytest.mark.skipif(torch.cuda.is_available(), reason="on a GPU the device's own cluster occupancy decides")
+def test_default_split_counts_follow_the_wave_cost_model(lib):
+    # Without a device the library assumes 152 SMs holding 152 / S clusters
+    # of S CTAs (S <= 8). Cost of S: waves * (19 + 5 * ceil(16 / S)) us, the
+    # cheapest S, then the fewest splits with the same tiles per CTA. The
+    # split count shows in the workspace: T * (H / 64) * S partials of
+    # 64 x 512 fp16 values plus 64 (m, l) pairs (none for S = 1).
+    per = 64 * 512 * 2 + 64 * 2 * 4
+
+    def splits(T, H=64):
+        n = lib.sparse_mla_decode_workspace_size(T, H, 2048, impl=lib.IMPL_TCGEN05)
+        assert n % (T * (H // 64) * per) == 0
+        return max(1, n // (T * (H // 64) * per))
+
+    assert splits(1) == 8      # one wave: 19 + 10
+    assert splits(15) == 8     # 15 clusters of 8 fit (19 resident)
+    assert splits(24) == 6     # 6 -> 3 tiles a CTA in one wave (34) beats 8 in two (58)
+    assert splits(35) == 4     # 38 clusters of 4 fit; 5 would need two waves
+    assert splits(64) == 2     # 59 against 98 for 3 splits
+    assert splits(128) == 1    # 99 against 118 for two waves of pairs
+    assert splits(160) == 2    # three waves of pairs (177) beat two of single CTAs (198)
+    assert splits(256) == 1    # 198 against 236
+    assert splits(320) == 2    # 295 against 297
+    assert splits(15, H=128) == 4  # 30 clusters: 5 splits of at most 4 tiles, reduced to 4
+
+
 def test_layered_calls_reject_bad_layers(lib):
     L = _raw(lib)
     P = ctypes.c_void_p
