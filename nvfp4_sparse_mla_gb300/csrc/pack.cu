@@ -38,6 +38,12 @@ nvfp4_pack_kernel(const __nv_bfloat16* __restrict__ latent, int64_t lat_stride,
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kPackWarps;
 
   for (int64_t n = static_cast<int64_t>(blockIdx.x) * kPackWarps + wib; n < n_tokens; n += nwarps) {
+    // the token's values are requested together with its slot (one memory
+    // round trip, not two); a token that is skipped leaves them unused
+    const uint4* src = reinterpret_cast<const uint4*>(latent + n * lat_stride + lane * 16);
+    const uint4 a = __ldg(src);
+    const uint4 b = __ldg(src + 1);
+    const uint32_t rw = __ldg(reinterpret_cast<const uint32_t*>(rope + n * rope_stride) + lane);
     const int64_t slot = __ldg(slot_mapping + n);
     if (slot < 0) continue;
     if (slot >= num_slots) {
@@ -45,9 +51,6 @@ nvfp4_pack_kernel(const __nv_bfloat16* __restrict__ latent, int64_t lat_stride,
       continue;
     }
     // ---- latent group `lane`
-    const uint4* src = reinterpret_cast<const uint4*>(latent + n * lat_stride + lane * 16);
-    const uint4 a = __ldg(src);
-    const uint4 b = __ldg(src + 1);
     const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
     float amax = 0.f;
 #pragma unroll
@@ -73,7 +76,6 @@ nvfp4_pack_kernel(const __nv_bfloat16* __restrict__ latent, int64_t lat_stride,
     *reinterpret_cast<uint2*>(row + 8 * lane) = make_uint2(codes[0], codes[1]);
     row[kScaleOff + lane] = static_cast<uint8_t>(sbyte);
     // ---- RoPE values 2*lane, 2*lane+1
-    const uint32_t rw = __ldg(reinterpret_cast<const uint32_t*>(rope + n * rope_stride) + lane);
     const uint16_t r8 = f32x2_to_e4m3x2(bf16_bits_to_f32(rw & 0xffffu), bf16_bits_to_f32(rw >> 16));
     *reinterpret_cast<uint16_t*>(row + kRopeOff + 2 * lane) = r8;
     __syncwarp();
@@ -112,15 +114,17 @@ fp8_pack_kernel(const __nv_bfloat16* __restrict__ latent, int64_t lat_stride, co
   uint8_t* row = rowbuf[wib];
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kPackWarps;
   for (int64_t n = static_cast<int64_t>(blockIdx.x) * kPackWarps + wib; n < n_tokens; n += nwarps) {
+    // values and slot in one round trip, as in nvfp4_pack_kernel
+    const uint4* src = reinterpret_cast<const uint4*>(latent + n * lat_stride + lane * 16);
+    const uint4 a = __ldg(src);
+    const uint4 b = __ldg(src + 1);
+    const uint32_t rw = __ldg(reinterpret_cast<const uint32_t*>(rope + n * rope_stride) + lane);
     const int64_t slot = __ldg(slot_mapping + n);
     if (slot < 0) continue;
     if (slot >= num_slots) {
       if (lane == 0) report_error(err_word, NVMLA_ERRW_PACK_SLOT, 1);
       continue;
     }
-    const uint4* src = reinterpret_cast<const uint4*>(latent + n * lat_stride + lane * 16);
-    const uint4 a = __ldg(src);
-    const uint4 b = __ldg(src + 1);
     const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
     uint32_t q[4];
 #pragma unroll
@@ -131,7 +135,6 @@ fp8_pack_kernel(const __nv_bfloat16* __restrict__ latent, int64_t lat_stride, co
       q[i] = lo | (hi << 16);
     }
     *reinterpret_cast<uint4*>(row + 16 * lane) = make_uint4(q[0], q[1], q[2], q[3]);
-    const uint32_t rw = __ldg(reinterpret_cast<const uint32_t*>(rope + n * rope_stride) + lane);
     *reinterpret_cast<uint16_t*>(row + kLatent + 2 * lane) =
         f32x2_to_e4m3x2(bf16_bits_to_f32(rw & 0xffffu), bf16_bits_to_f32(rw >> 16));
     __syncwarp();
