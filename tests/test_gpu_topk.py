@@ -48,7 +48,8 @@ def test_heavy_ties(lib, cuda):
 
 
 def test_many_equal_keys_per_chunk(lib, cuda):
-    # more equal keys in the chosen bin than a CTA keeps in shared memory
+    # more keys in the chosen bin than rank 0's pool holds, and more per
+    # thread than its list holds: the cluster-wide passes over the chunk
     check(lib, cuda, np.zeros((2, 200_000)), 2048)
     rng = np.random.default_rng(26)
     check(lib, cuda, rng.integers(0, 4, (3, 200_000)).astype(np.float64), 2048)
