@@ -47,6 +47,16 @@ def test_heavy_ties(lib, cuda):
     check(lib, cuda, s, 2048)
 
 
+def test_ties_inside_the_pool(lib, cuda):
+    # ~2,500 keys tied at the top value: the pool takes them all and the
+    # list ends with the lowest 2,048 of their positions
+    rng = np.random.default_rng(31)
+    check(lib, cuda, rng.integers(0, 20, (3, 50_000)).astype(np.float64), 2048)
+    # scores on a 0.001 grid: the threshold key has a few exact copies among
+    # the last keys rank 0 counts
+    check(lib, cuda, np.round(rng.standard_normal((3, 200_000)), 3), 2048)
+
+
 def test_many_equal_keys_per_chunk(lib, cuda):
     # more keys in the chosen bin than rank 0's pool holds, and more per
     # thread than its list holds: the cluster-wide passes over the chunk
