@@ -162,11 +162,39 @@ class ClockSampler:
                 "reasons": reasons}
 
 
+def strip_comments(src):
+    """C/C++/CUDA source without its comments and blank lines, trailing spaces
+    removed: what a comment-only edit leaves unchanged."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c == '"' or c == "'":  # a literal: copied through, escapes included
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    lines = ("".join(out)).split("\n")
+    return "\n".join(l.rstrip() for l in lines if l.strip())
+
+
 def source_hash(names):
+    """Hash of a kernel's source files, comments left out: the traffic record
+    stays valid across comment-only edits and lapses on any code change."""
     h = hashlib.sha256()
     for n in names:
-        with open(os.path.join(ROOT, "nvfp4_sparse_mla_gb300", "csrc", n), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "nvfp4_sparse_mla_gb300", "csrc", n), encoding="utf-8") as f:
+            h.update(strip_comments(f.read()).encode("utf-8"))
     return h.hexdigest()[:16]
 
 

@@ -12,43 +12,53 @@
 // contribute nothing).
 //
 // One cluster = one query token x 64 heads; its S CTAs take contiguous
-// ranges of the token's slots, in tiles of 128 rows. Roles in a CTA
-// (17 warps):
+// ranges of the token's slots, in tiles of 128 rows. Both contractions run as
+// tcgen05.mma kind::f16 (M = 128, N = 64, K = 16) in swap-AB orientation, the
+// 64 heads being N:
+//   S^T[128 rows, 64 heads]  = K[128 x 576] . Q^T     A: K in TMEM, B: Q in shared memory
+//   O^T[512 dims, 64 heads] += V^T[512 x 128] . P^T   A: V^T, B: P^T, both in shared memory
+// TMEM (512 columns): S^T in columns 0-63, O^T in 64-319 (4 blocks of 128
+// dims), and a ring of 6 K slots of 32 columns (64 fp16 dims x 128 rows) in
+// 320-511. A tile's K is 9 chunks of 64 dims (8 latent, 1 RoPE): QK batch A
+// takes chunk uses 0-5 in slots 0-5, batch B uses 6-8 in slots 0-2, once
+// batch A's MMAs have read them.
 //
-//   warps 0-7   unpack: thread (row r, half h) loads the half of its cache
-//               row it converts -- the 128 code bytes of latent dims
-//               256h..256h+255, their 16 scale bytes and RoPE values
-//               32h..32h+31 -- with six 32- / 16-byte loads (176 bytes), and
-//               writes fp16 operands (E2M1 x E4M3 is exact in fp16) into
-//               shared memory, 128B-swizzled: at step j latent chunk 4h + j
-//               (64 dims), then its half of the RoPE chunk. Each piece of the
-//               next tile's row is requested as soon as the current tile no
-//               longer needs its registers.
-//   warp 16     MMA issue (one thread) and TMEM allocation. M = 128 always:
-//                 S^T[128 rows, 64 heads]  = K[128 x 576] . Q^T   (9 chunks)
-//                 O^T[512 dims, 64 heads] += V^T[512 x 128] . P^T (4 blocks)
-//               QK of chunk pair (j, j + 4) starts as soon as step j of the
-//               unpack lands. The latent chunks are unpacked once: a K-major
-//               128-row x 64-dim chunk is byte for byte the MN-major layout
-//               of V^T for those 64 value dims, so PV block j reads chunks j
-//               and j + 4 (dims 64j.. and 256 + 64j..) and its completion
-//               frees exactly what step j of the next tile's unpack writes.
-//               A tcgen05.mma issue holds the issuing thread for about the
-//               instruction's run time, hence a warp of its own.
+// Roles in a CTA (18 warps, 96 registers a thread):
+//
+//   warps 0-7   unpack: thread (row r, half h) holds the half of its cache
+//               row it converts -- the code bytes of latent dims
+//               256h..256h+255 and their 16 scale bytes, half 0 also the
+//               RoPE bytes -- and writes fp16 values (E2M1 x E4M3 is exact in
+//               fp16) into the K ring with tcgen05.st. Each piece of the next
+//               tile's row is requested as soon as the current tile no longer
+//               needs its registers.
 //   warps 8-15  softmax: warp (lane quadrant q, head half g) owns TMEM lanes
-//               32q..32q+31 (= rows) and heads 32g..32g+31. The running
-//               maximum of every head stays fixed while no score exceeds it
-//               by more than 2^8 (P stays below 256, safe in fp16); only a
-//               tile that does (always the first) pays for the exact
-//               cross-row maximum and the rescale of O^T in TMEM. Row sums
-//               accumulate per thread and are reduced across rows once, at
-//               the end. P^T goes to shared memory in place of the RoPE
-//               chunk, which QK no longer needs.
+//               32q..32q+31 (= rows) and heads 32g..32g+31. It copies the
+//               latent chunks out of the K ring into the V tile in shared
+//               memory (128B-swizzled: a K-major 128-row chunk of 64 dims is
+//               the MN-major layout of V^T for those dims), reads S^T and
+//               writes P^T to shared memory. A head's running maximum starts,
+//               on the first tile, at the largest score of rows 0, 32, 64 and
+//               96, and stays fixed while no score exceeds it by more than
+//               2^15 (P stays below 2^15, safe in fp16); only a tile that
+//               does pays for the exact cross-row maximum and the rescale of
+//               O^T in TMEM. Row sums accumulate per thread and are reduced
+//               across rows once, at the end.
+//   warp 16     issues the QK MMAs (one thread); allocates and frees TMEM.
+//   warp 17     issues the PV MMAs (one thread). PV block j reads V chunks j
+//               and j + 4 (dims 64j.. and 256 + 64j..). Blocks 0-1 commit on
+//               their own, so the next tile's V copy into chunks 0, 1, 4 and
+//               5 starts while blocks 2-3 run.
+//
+// The next tile's unpack and QK overlap the current tile's softmax and PV.
+// The FP8-row variant loads 576-byte E4M3 rows and converts them without
+// scales; everything from the K ring on is shared.
 //
 // Start-up issues the dependent loads first (slot list and sequence ->
 // block table and sequence length -> rows of the first tile, three levels;
-// L2 prefetch of the later tiles' rows) and converts the query block while
-// they are in flight.
+// the rows are requested before the sequence length arrives and ignored if
+// they lie past it) and converts the query block (bf16 -> fp16) while they
+// are in flight; the later tiles' rows are prefetched into L2 after it.
 //
 // Combine: a token's only CTA writes out / lse itself. With S CTAs, each
 // normalises its O^T block by block as PV finishes (O / l, fp16, in the
@@ -61,8 +71,8 @@
 // memory does.
 //
 // Shared memory: query block (72 KB) + slot list (8 KB), later the combine's
-// receive buffer; latent tile (128 KB), later the partial staging; RoPE/P^T
-// chunk (16 KB), later the combine weights. TMEM: S^T 64 columns, O^T 4 x 64.
+// receive buffer; V tile (128 KB), later the partial staging; P^T (16 KB),
+// later the combine weights.
 // Every mbarrier wait is bounded: on timeout the CTA sets
 // NVMLA_ERRW_WAIT_TIMEOUT, drains its MMAs and still takes part in the
 // cluster barrier, so that every CTA of the cluster exits.
