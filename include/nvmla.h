@@ -88,6 +88,8 @@ typedef enum {
 #define NVMLA_ROPE_DIM 64
 #define NVMLA_MAX_TOPK 2048
 #define NVMLA_MAX_HEADS 128
+#define NVMLA_MAX_TOKENS 65535          /* query tokens per call (T) */
+#define NVMLA_MAX_TOPK_COLS (1 << 29)   /* candidates per row of nvmla_topk_select */
 
 /*
  * nvfp4_mla_pack -- write n_tokens rows into the paged cache.
@@ -134,7 +136,8 @@ nvmla_status nvfp4_mla_pack(const void* latent_bf16, int64_t latent_stride,
  *                every token belongs to sequence 0).
  *   seq_lens     (device, nullable) int32 [num_seqs] context lengths (NULL:
  *                positions are only checked against the block-table width).
- *   T, H         query tokens (>= 0) and heads (multiple of 16, <= 128).
+ *   T, H         query tokens (0 .. NVMLA_MAX_TOKENS) and heads (multiple of
+ *                16, <= 128).
  *   topk         slots per token, 1..2048.
  *   sm_scale     softmax scale applied to q.k.
  *   out          (device) bf16 [T][H][512]: sum_k softmax_k * V_k.
@@ -327,7 +330,9 @@ size_t sparse_mla_decode_fp8rows_workspace_size(int32_t T, int32_t H, int32_t to
  *
  *   scores     (device) fp32 [T][row_stride], 4-byte aligned; token t's
  *              candidates are positions 0 .. length_t - 1 of row t.
- *   ncols      columns that hold scores (row_stride >= ncols >= 0).
+ *   ncols      columns that hold scores (row_stride >= ncols >= 0,
+ *              ncols <= NVMLA_MAX_TOPK_COLS).
+ *   T          rows (0 .. NVMLA_MAX_TOKENS).
  *   lengths    (device, nullable) int32 [T]: length_t, clamped to
  *              [0, ncols]; NULL means ncols for every token.
  *   topk       1..2048, the list length.

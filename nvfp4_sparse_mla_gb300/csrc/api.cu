@@ -85,6 +85,7 @@ struct DecodeShape {
 
 nvmla_status check_shape(int32_t T, int32_t H, int32_t topk, float sm_scale) {
   if (T < 0) return fail(NVMLA_ERR_INVALID_ARG, "T = %d must be >= 0", T);
+  if (T > NVMLA_MAX_TOKENS) return fail(NVMLA_ERR_UNSUPPORTED, "T = %d exceeds %d", T, NVMLA_MAX_TOKENS);
   if (H <= 0 || H % 16 != 0) return fail(NVMLA_ERR_UNSUPPORTED, "H = %d must be a positive multiple of 16", H);
   if (H > NVMLA_MAX_HEADS) return fail(NVMLA_ERR_UNSUPPORTED, "H = %d exceeds %d", H, NVMLA_MAX_HEADS);
   if (topk < 1 || topk > NVMLA_MAX_TOPK) return fail(NVMLA_ERR_UNSUPPORTED, "topk = %d must be in [1, %d]", topk, NVMLA_MAX_TOPK);
@@ -395,7 +396,9 @@ nvmla_status nvmla_topk_select(const float* scores, int64_t row_stride, int32_t 
   if (T < 0) return fail(NVMLA_ERR_INVALID_ARG, "T = %d must be >= 0", T);
   if (topk < 1 || topk > NVMLA_MAX_TOPK)
     return fail(NVMLA_ERR_UNSUPPORTED, "topk = %d must be in [1, %d]", topk, NVMLA_MAX_TOPK);
+  if (T > NVMLA_MAX_TOKENS) return fail(NVMLA_ERR_UNSUPPORTED, "T = %d exceeds %d", T, NVMLA_MAX_TOKENS);
   if (ncols < 0) return fail(NVMLA_ERR_INVALID_ARG, "ncols = %d must be >= 0", ncols);
+  if (ncols > NVMLA_MAX_TOPK_COLS) return fail(NVMLA_ERR_UNSUPPORTED, "ncols = %d exceeds %d", ncols, NVMLA_MAX_TOPK_COLS);
   if (row_stride < ncols) return fail(NVMLA_ERR_INVALID_ARG, "row_stride must be >= ncols");
   if (T == 0) return NVMLA_OK;
   if ((!scores && ncols > 0) || !topk_idx) return fail(NVMLA_ERR_INVALID_ARG, "null scores/topk_idx");

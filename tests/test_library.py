@@ -172,6 +172,16 @@ def test_topk_select_rejects_bad_arguments(lib):
     assert L.nvmla_topk_select(P(0x10002), 100, 100, None, 3, 2048, ok, None) == 1
     assert L.nvmla_topk_select(ok, 100, 100, None, -1, 2048, ok, None) == 1
     assert L.nvmla_topk_select(ok, 100, 100, None, 0, 2048, ok, None) == 0     # no-op
+    assert L.nvmla_topk_select(ok, 100, 100, None, 65536, 2048, ok, None) == 2  # T beyond the grid
+    big = (1 << 29) + 1
+    assert L.nvmla_topk_select(ok, big, big, None, 3, 2048, ok, None) == 2     # row too long
+
+
+def test_decode_rejects_too_many_tokens(lib):
+    L = _raw(lib)
+    ok = ctypes.c_void_p(0x10000)
+    args = [ok, ok, ok, 10, ok, 1, 4, ok, 2048, None, None, 65536, 64, 0.1, ok, ok, None, 0, None, None]
+    assert L.sparse_mla_decode(*args) == 2
 
 
 def test_fp8_cache_calls_reject_bad_arguments(lib):
