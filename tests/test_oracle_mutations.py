@@ -158,3 +158,102 @@ def test_missing_saturation(monkeypatch):
 
     monkeypatch.setattr(formats, "e2m1_encode_scaled", mutated)
     assert fails(F.check_e2m1_encode_exhaustive)
+
+
+# ---- the top-k list builder, the multi-layer cache and the FP8 cache
+
+import test_oracle_fp8cache as FC  # noqa: E402
+import test_oracle_layered as LY  # noqa: E402
+import test_oracle_topk as TK  # noqa: E402
+from oracle import fp8cache, layered, topk  # noqa: E402
+
+
+def _topk_variant(kind):
+    def f(scores, k, lengths=None):
+        s = np.asarray(scores, dtype=np.float64)
+        T, ncols = s.shape
+        out = np.full((T, k), -1, dtype=np.int64)
+        for t in range(T):
+            L = ncols if (lengths is None or kind == "lengths_ignored") else int(min(max(int(lengths[t]), 0), ncols))
+            kk = min(k, L)
+            pos = np.arange(L)
+            if kind == "raw_bits":  # -0.0 ranked below +0.0, as its bit pattern does
+                b = s[t, :L].astype(np.float32).view(np.uint32).astype(np.int64)
+                key = np.where(b & 0x80000000, 0xFFFFFFFF - b, b | 0x80000000)
+                order = np.lexsort((pos, -key))
+            elif kind == "ties_high":
+                order = np.lexsort((-pos, -(s[t, :L] + 0.0)))
+            else:
+                order = np.lexsort((pos, -(s[t, :L] + 0.0)))
+            chosen = pos[order[:kk]]
+            out[t, :kk] = chosen if kind == "unsorted" else np.sort(chosen)
+        return out
+    return f
+
+
+@pytest.mark.parametrize("kind,checks", [
+    ("ties_high", (TK.test_equal_scores_take_the_lowest_positions, lambda: TK.test_agrees_with_heapq(1))),
+    ("unsorted", (TK.test_increasing_scores_take_the_last_positions, TK.test_chosen_scores_dominate_the_rest)),
+    ("raw_bits", (TK.test_negative_zero_ties_with_positive_zero,)),
+    ("lengths_ignored", (TK.test_short_lists_are_padded,)),
+])
+def test_topk_mistakes(monkeypatch, kind, checks):
+    monkeypatch.setattr(topk, "topk_select", _topk_variant(kind))
+    assert fails(*checks)
+
+
+def test_layer_off_by_one(monkeypatch):
+    real = layered.layer_view
+    monkeypatch.setattr(layered, "layer_view", lambda cache, layer: real(cache, (layer + 1) % cache.shape[1]))
+    assert fails(LY.test_rows_sit_at_the_layout_formula, LY.test_layered_decode_is_the_one_layer_decode)
+
+
+def test_token_major_row_formula(monkeypatch):
+    monkeypatch.setattr(layered, "row_byte_offset",
+                        lambda block, layer, token, num_layers: ((block * 64 + token) * num_layers + layer) * 352)
+    assert fails(LY.test_rows_sit_at_the_layout_formula)
+
+
+def test_pack_writes_every_layer(monkeypatch):
+    def mutated(latent, rope, slot_mapping, cache, layer):
+        one = layered.layer_view(cache, layer)
+        pack.pack_into_cache(latent, rope, slot_mapping, one)
+        cache[:] = one[:, None]
+        return cache
+
+    monkeypatch.setattr(layered, "pack_into_layered_cache", mutated)
+    assert fails(LY.test_packing_a_layer_leaves_the_others_alone)
+
+
+def test_fp8_row_halves_swapped(monkeypatch):
+    def mutated(latent, rope):
+        row = np.empty((np.asarray(latent).shape[0], 576), dtype=np.uint8)
+        row[:, :64] = formats.e4m3_encode(np.asarray(rope, dtype=np.float64))
+        row[:, 64:] = formats.e4m3_encode(np.asarray(latent, dtype=np.float64))
+        return row
+
+    monkeypatch.setattr(fp8cache, "pack_rows", mutated)
+    assert fails(FC.test_exact_values_round_trip)
+
+
+def test_fp8_nan_instead_of_saturation(monkeypatch):
+    real = fp8cache.pack_rows
+
+    def mutated(latent, rope):
+        row = real(latent, rope)
+        vals = np.concatenate([np.asarray(latent, dtype=np.float64), np.asarray(rope, dtype=np.float64)], axis=1)
+        over = np.abs(vals) > 448
+        return np.where(over, np.where(vals < 0, 0xFF, 0x7F), row).astype(np.uint8)
+
+    monkeypatch.setattr(fp8cache, "pack_rows", mutated)
+    assert fails(FC.test_saturation)
+
+
+def test_topk_variant_without_a_mistake_passes_every_pin(monkeypatch):
+    # (the control: the mutations above fail the pins for their mistake, not
+    # for a difference in how the variant is written)
+    monkeypatch.setattr(topk, "topk_select", _topk_variant("none"))
+    checks = [TK.test_equal_scores_take_the_lowest_positions, TK.test_increasing_scores_take_the_last_positions,
+              TK.test_short_lists_are_padded, TK.test_chosen_scores_dominate_the_rest,
+              TK.test_negative_zero_ties_with_positive_zero] + [lambda s=s: TK.test_agrees_with_heapq(s) for s in (1, 2, 3)]
+    assert not fails(*checks)
