@@ -9,8 +9,8 @@ every call raises.
 
 Calls (same names as the C ABI, see include/nvmla.h):
 
-* ``nvfp4_mla_pack(latent, rope, slot_mapping, cache)``
-* ``sparse_mla_decode(q_latent, q_rope, cache, block_table, topk_idx, sm_scale, ...)``
+* ``nvfp4_mla_pack(latent, rope, slot_mapping, cache)`` (also ``pack``)
+* ``sparse_mla_decode(q_latent, q_rope, cache, block_table, topk_idx, sm_scale, ...)`` (also ``decode``)
 * ``sparse_mla_decode_noalloc(q_latent, q_rope, cache, block_table, topk_idx, sm_scale, out, lse, ...)``
   (the same decode with the library's own split scratch; allocates nothing)
 * ``nvfp4_mla_pack_layered(latent, rope, slot_mapping, cache, layer)`` and
@@ -40,6 +40,7 @@ __all__ = [
     "nvfp4_mla_pack_layered", "sparse_mla_decode_layered", "nvmla_topk_select",
     "fp8_mla_pack", "sparse_mla_decode_fp8cache",
     "IMPL_AUTO", "IMPL_MMA", "IMPL_TCGEN05", "ROW_BYTES", "FP8_ROW_BYTES", "PAGE_TOKENS",
+    "pack", "decode",
 ]
 
 ROW_BYTES = 352
@@ -496,3 +497,8 @@ def sparse_mla_decode_fp8rows(q_latent: torch.Tensor, q_rope: torch.Tensor, fp8_
                                          float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
                                          _ptr(err_word), opts, _stream(q_latent, stream)))
     return out, lse
+
+
+# short names of the two calls of the path (the same functions)
+pack = nvfp4_mla_pack
+decode = sparse_mla_decode

@@ -132,6 +132,11 @@ def test_default_split_counts_follow_the_wave_cost_model(lib):
     assert splits(15, H=128) == 4  # 30 clusters: 5 splits of at most 4 tiles, reduced to 4
 
 
+def test_short_names_are_the_calls(lib):
+    assert lib.pack is lib.nvfp4_mla_pack and lib.decode is lib.sparse_mla_decode
+    assert {"pack", "decode"} <= set(lib.__all__)
+
+
 def test_layered_calls_reject_bad_layers(lib):
     L = _raw(lib)
     P = ctypes.c_void_p
