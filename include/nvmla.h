@@ -346,9 +346,9 @@ size_t sparse_mla_decode_fp8rows_workspace_size(int32_t T, int32_t H, int32_t to
  *
  * Each row runs on one cluster of 8 CTAs. Rows of up to 262,144 candidates
  * are read from global memory once (each CTA keeps its eighth in shared
- * memory); longer rows, or rows whose k-th largest score is shared with more
- * than ~8,000 others, take slower passes over global memory, with the same
- * result.
+ * memory). Slower passes, with the same result, serve longer rows and rows
+ * where more than 8,192 scores share the k-th largest score's sign,
+ * exponent and two leading mantissa bits.
  */
 nvmla_status nvmla_topk_select(const float* scores, int64_t row_stride, int32_t ncols,
                                const int32_t* lengths, int32_t T, int32_t topk,
