@@ -1272,6 +1272,11 @@ namespace {
 // Per-device launch setup of the kernel: its shared-memory size, and for
 // every cluster size S how many clusters of S CTAs can be resident at once
 // (0: S cannot be launched).
+// Per-device launch set-up, filled on the first call on each device. Two host
+// threads making their first call on one device at once may both fill it,
+// with the same values; one that sees `ready` before the occupancy table
+// (the flag is a plain bool) reads zeros there and takes one split for that
+// call, which is slower but gives the same results.
 struct TcDevice {
   bool ready = false;
   int max_active[tc::kMaxCluster + 1] = {0};
