@@ -176,9 +176,17 @@ typedef enum {
 } nvmla_impl;
 
 typedef struct {
-  int32_t impl;       /* nvmla_impl                                        */
-  int32_t num_splits; /* key splits per token; 0 = heuristic               */
+  int32_t impl;        /* nvmla_impl                                       */
+  int32_t num_splits;  /* key splits per token; 0 = heuristic              */
+  int32_t debug_flags; /* NVMLA_DEBUG_* test hooks; 0 in normal use        */
 } nvmla_decode_options;
+
+/* Test hook of the tcgen05 kernel: its wait for the softmax's P^T gives up
+ * at once, as a bounded wait that ran out would. The call then returns
+ * NVMLA_OK, sets NVMLA_ERRW_WAIT_TIMEOUT in err_word, leaves out and lse
+ * undefined, and every CTA exits normally (its issued MMAs drained, TMEM
+ * freed, every cluster barrier met). Other kernels ignore it. */
+#define NVMLA_DEBUG_FORCE_WAIT_TIMEOUT 0x1
 
 /* sparse_mla_decode with explicit options (NULL options = defaults). */
 nvmla_status sparse_mla_decode_ex(const void* q_latent, const void* q_rope,
@@ -196,6 +204,14 @@ nvmla_status sparse_mla_decode_ex(const void* q_latent, const void* q_rope,
 /* Workspace for sparse_mla_decode_ex with the given options. */
 size_t sparse_mla_decode_workspace_size_ex(int32_t T, int32_t H, int32_t topk,
                                            const nvmla_decode_options* opts);
+
+/* Key splits per token sparse_mla_decode_ex takes for (T, H, topk) with the
+ * given options (NULL = defaults) on the current device, given enough
+ * workspace: the CTAs that share one token's slots [Serving, "A native
+ * NVFP4 sparse-MLA decode kernel": a cluster of cooperating SMs per query
+ * token]. 0 for a shape the call rejects. Host-only. */
+int32_t sparse_mla_decode_splits(int32_t T, int32_t H, int32_t topk,
+                                 const nvmla_decode_options* opts);
 
 /*
  * Block-major multi-layer caches.
@@ -243,20 +259,26 @@ nvmla_status sparse_mla_decode_layered(const void* q_latent, const void* q_rope,
  * argument. The pages describe no such call: it exists for callers that
  * cannot allocate GPU memory (an engine whose memory pool owns the whole
  * GPU, a replayed fixed launch sequence, a C caller with no allocator). The
- * call allocates nothing: the split partials go to a scratch array of
- * sparse_mla_decode_noalloc_max_scratch() bytes (16 MiB) in device memory
- * owned by the library, reserved on each device where the library's code
- * loads and held until the process exits.
+ * call allocates nothing: split partials that need global memory go to a
+ * scratch array of sparse_mla_decode_noalloc_max_scratch() bytes (16 MiB) in
+ * device memory owned by the library, reserved on each device where the
+ * library's code loads and held until the process exits.
  *
  *   Arguments, results and err_word: as sparse_mla_decode.
  *   Same kernels and split count as sparse_mla_decode given a workspace of
  *   sparse_mla_decode_workspace_size(T, H, topk) bytes, hence the same output
  *   bits.
- *   Returns NVMLA_ERR_WORKSPACE, launching nothing, when that size exceeds the
- *   scratch (H a multiple of 64 always fits on GPUs with up to 254 SMs; some
- *   other H at large T do not).
+ *   Scratch needed: none when H is a multiple of 64 (the tcgen05 kernel
+ *   combines its splits in shared memory). Otherwise the mma.sync kernel's
+ *   T * S * H * (512 + 2) * 4 bytes, S its split count, and T * S <=
+ *   floor(SMs / ceil(H / 64)): at most 15.0 MB for every H but 112 on a
+ *   152-SM GB300 (17.5 MB for H = 112). Returns NVMLA_ERR_WORKSPACE,
+ *   launching nothing, when the need exceeds the scratch.
  *   The first call on each device looks up the scratch's address
- *   (cudaGetSymbolAddress); make it before any stream capture on that device.
+ *   (cudaGetSymbolAddress) and keeps it; make that call before any stream
+ *   capture on the device. The address is that of the device's current
+ *   context: after cudaDeviceReset (or any destruction of the primary
+ *   context) the process must not call this function on that device again.
  *   The scratch is shared: calls whose work overlaps on the GPU (different
  *   streams, threads or processes sharing one context) race on it and give
  *   wrong results. Order such calls on one stream or by events.

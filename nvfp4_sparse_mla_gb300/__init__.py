@@ -47,6 +47,7 @@ ROW_BYTES = 352
 FP8_ROW_BYTES = 576
 PAGE_TOKENS = 64
 IMPL_AUTO, IMPL_MMA, IMPL_TCGEN05 = 0, 1, 2
+DEBUG_FORCE_WAIT_TIMEOUT = 0x1  # NVMLA_DEBUG_FORCE_WAIT_TIMEOUT (a test hook)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_NAME = "libnvmla.so"
@@ -63,7 +64,7 @@ class NvmlaError(RuntimeError):
 
 
 class _Options(ctypes.Structure):
-    _fields_ = [("impl", ctypes.c_int32), ("num_splits", ctypes.c_int32)]
+    _fields_ = [("impl", ctypes.c_int32), ("num_splits", ctypes.c_int32), ("debug_flags", ctypes.c_int32)]
 
 
 def library_path() -> str:
@@ -90,6 +91,7 @@ def load():
                                             P, OPT, P]),
         "sparse_mla_decode_workspace_size": (SZ, [I32, I32, I32]),
         "sparse_mla_decode_workspace_size_ex": (SZ, [I32, I32, I32, OPT]),
+        "sparse_mla_decode_splits": (I32, [I32, I32, I32, OPT]),
         "sparse_mla_decode_noalloc": (I32, [P, P, P, I64, P, I32, I32, P, I32, P, P, I32, I32, F, P, P, P, P]),
         "sparse_mla_decode_noalloc_max_scratch": (SZ, []),
         "nvfp4_stage_dequant_fp8": (I32, [P, I64, P, I32, I32, P, I32, P, P, I32, P, P, P, P]),
@@ -146,10 +148,10 @@ def _need(t, name, dtype, dims=None, contiguous=True):
         raise ValueError(f"{name} must be contiguous")
 
 
-def _opts(impl, num_splits):
-    if impl is None and num_splits is None:
+def _opts(impl, num_splits, debug_flags=None):
+    if impl is None and num_splits is None and not debug_flags:
         return None
-    return ctypes.pointer(_Options(int(impl or 0), int(num_splits or 0)))
+    return ctypes.pointer(_Options(int(impl or 0), int(num_splits or 0), int(debug_flags or 0)))
 
 
 def nvfp4_mla_pack(latent: torch.Tensor, rope: torch.Tensor, slot_mapping: torch.Tensor, cache: torch.Tensor,
@@ -356,6 +358,13 @@ def sparse_mla_decode_workspace_size(T: int, H: int, topk: int, impl=None, num_s
     return int(lib.sparse_mla_decode_workspace_size_ex(T, H, topk, _opts(impl, num_splits)))
 
 
+def sparse_mla_decode_splits(T: int, H: int, topk: int, impl=None, num_splits=None) -> int:
+    """Key splits per token the decode takes for (T, H, topk) on the current
+    device (0 for a shape it rejects)."""
+    lib = load()
+    return int(lib.sparse_mla_decode_splits(T, H, topk, _opts(impl, num_splits)))
+
+
 def sparse_mla_decode_fp8rows_workspace_size(T: int, H: int, topk: int, impl=None, num_splits=None) -> int:
     lib = load()
     return int(lib.sparse_mla_decode_fp8rows_workspace_size(T, H, topk, _opts(impl, num_splits)))
@@ -365,9 +374,11 @@ def sparse_mla_decode(q_latent: torch.Tensor, q_rope: torch.Tensor, cache: torch
                       topk_idx: torch.Tensor, sm_scale: float, out: Optional[torch.Tensor] = None,
                       lse: Optional[torch.Tensor] = None, q_seq_idx: Optional[torch.Tensor] = None,
                       seq_lens: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-                      err_word: Optional[torch.Tensor] = None, impl=None, num_splits=None, stream=None):
+                      err_word: Optional[torch.Tensor] = None, impl=None, num_splits=None, stream=None,
+                      debug_flags=None):
     """Sparse MLA decode over the NVFP4 cache. Returns (out bf16 [T,H,512],
-    lse fp32 [T,H])."""
+    lse fp32 [T,H]). debug_flags: the NVMLA_DEBUG_* test hooks (None in
+    normal use)."""
     _need(q_latent, "q_latent", torch.bfloat16, 3)
     _need(q_rope, "q_rope", torch.bfloat16, 3)
     _need(cache, "cache", torch.uint8, 3)
@@ -391,7 +402,7 @@ def sparse_mla_decode(q_latent: torch.Tensor, q_rope: torch.Tensor, cache: torch
     _need(out, "out", torch.bfloat16, 3)
     _need(lse, "lse", torch.float32, 2)
     topk = topk_idx.shape[1]
-    opts = _opts(impl, num_splits)
+    opts = _opts(impl, num_splits, debug_flags)
     lib = load()
     if workspace is None:
         nbytes = int(lib.sparse_mla_decode_workspace_size_ex(T, H, topk, opts))

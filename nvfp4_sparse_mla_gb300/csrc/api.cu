@@ -34,7 +34,8 @@ int tc_default_splits(int T, int H, int topk, int num_sms);
 int tc_max_splits();
 size_t tc_workspace_bytes(int T, int H, int splits);
 cudaError_t launch_decode_tc(int fmt, const void*, const void*, const uint8_t*, const RowSelect&, const int32_t*,
-                             int, int, int, float, void*, float*, void*, int, int32_t*, cudaStream_t);
+                             int, int, int, float, void*, float*, void*, int, int32_t*, cudaStream_t,
+                             uint32_t p_wait_ns, int force_p_timeout);
 
 namespace {
 
@@ -144,6 +145,11 @@ int pick_impl_fp8(const nvmla_decode_options* opts, int H) {
   return tc_fp8_supported(H) ? NVMLA_IMPL_TCGEN05 : NVMLA_IMPL_MMA;
 }
 
+// The test hook that makes the tcgen05 kernel's wait for P^T give up at once.
+int force_timeout(const nvmla_decode_options* opts) {
+  return (opts && (opts->debug_flags & NVMLA_DEBUG_FORCE_WAIT_TIMEOUT)) ? 1 : 0;
+}
+
 // Split count for the mma kernel that fits the workspace (explicit requests
 // must fit; the heuristic falls back to fewer splits).
 int impl_tile(int impl) { return impl == NVMLA_IMPL_TCGEN05 ? 128 : 64; }
@@ -206,7 +212,7 @@ const char* nvmla_status_string(nvmla_status s) {
 
 const char* nvmla_last_error(void) { return g_last_error.c_str(); }
 
-int32_t nvmla_version(void) { return 100; }
+int32_t nvmla_version(void) { return 200; }
 
 uint64_t nvmla_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
@@ -261,6 +267,17 @@ size_t sparse_mla_decode_workspace_size_ex(int32_t T, int32_t H, int32_t topk, c
   return workspace_bytes(impl, T, H, s);
 }
 
+int32_t sparse_mla_decode_splits(int32_t T, int32_t H, int32_t topk, const nvmla_decode_options* opts) {
+  if (T <= 0 || H <= 0 || H % 16 != 0 || H > NVMLA_MAX_HEADS || topk < 1 || topk > NVMLA_MAX_TOPK) return 0;
+  const int impl = pick_impl(opts, H);
+  if (impl == NVMLA_IMPL_TCGEN05 && !tc_supported(H)) return 0;
+  const int tiles = (topk + impl_tile(impl) - 1) / impl_tile(impl);
+  int s = (opts && opts->num_splits > 0) ? opts->num_splits : default_splits(impl, T, H, topk);
+  if (s > tiles) s = tiles;
+  if (s < 1) s = 1;
+  return s;
+}
+
 size_t sparse_mla_decode_workspace_size(int32_t T, int32_t H, int32_t topk) {
   return sparse_mla_decode_workspace_size_ex(T, H, topk, nullptr);
 }
@@ -289,7 +306,8 @@ nvmla_status decode_impl(const void* q_latent, const void* q_rope, const uint8_t
   if ((s = check_cache(cache, num_blocks, block_table, num_seqs, max_pages_per_seq, topk_idx)) != NVMLA_OK) return s;
   if ((s = check_layers(num_blocks, num_layers, layer)) != NVMLA_OK) return s;
   if (err_word && !aligned(err_word, 4)) return fail(NVMLA_ERR_INVALID_ARG, "err_word must be 4-byte aligned");
-  if (opts && (opts->impl < 0 || opts->impl > NVMLA_IMPL_TCGEN05 || opts->num_splits < 0))
+  if (opts && (opts->impl < 0 || opts->impl > NVMLA_IMPL_TCGEN05 || opts->num_splits < 0 ||
+               (opts->debug_flags & ~NVMLA_DEBUG_FORCE_WAIT_TIMEOUT) != 0))
     return fail(NVMLA_ERR_INVALID_ARG, "bad options");
   RowSelect sel{topk_idx, block_table, q_seq_idx, seq_lens, num_blocks * NVMLA_PAGE_TOKENS, topk, max_pages_per_seq,
                 num_seqs, NVMLA_PAGE_TOKENS * num_layers};
@@ -302,7 +320,7 @@ nvmla_status decode_impl(const void* q_latent, const void* q_rope, const uint8_t
   if ((s = pick_splits(impl, opts, T, H, topk, workspace_bytes, workspace, &splits)) != NVMLA_OK) return s;
   if (impl == NVMLA_IMPL_TCGEN05) {
     return counted(launch_decode_tc(0, q_latent, q_rope, rows, sel, nullptr, T, H, topk, sm_scale, out, lse,
-                                    workspace, splits, err_word, st),
+                                    workspace, splits, err_word, st, 0, force_timeout(opts)),
                    1, "sparse_mla_decode (tcgen05) launch");
   }
   return counted(launch_decode_mma(0, q_latent, q_rope, rows, sel, nullptr, T, H, topk, sm_scale, out, lse,
@@ -376,18 +394,19 @@ nvmla_status sparse_mla_decode_fp8cache(const void* q_latent, const void* q_rope
   if ((s = check_queries(q_latent, q_rope, out, lse)) != NVMLA_OK) return s;
   if ((s = check_cache(cache, num_pages, block_table, num_seqs, max_pages_per_seq, topk_idx)) != NVMLA_OK) return s;
   if (err_word && !aligned(err_word, 4)) return fail(NVMLA_ERR_INVALID_ARG, "err_word must be 4-byte aligned");
-  if (opts && (opts->impl < 0 || opts->impl > NVMLA_IMPL_TCGEN05 || opts->num_splits < 0))
+  if (opts && (opts->impl < 0 || opts->impl > NVMLA_IMPL_TCGEN05 || opts->num_splits < 0 ||
+               (opts->debug_flags & ~NVMLA_DEBUG_FORCE_WAIT_TIMEOUT) != 0))
     return fail(NVMLA_ERR_INVALID_ARG, "bad options");
   if ((opts && opts->impl == NVMLA_IMPL_MMA) || !tc_supported(H))
     return fail(NVMLA_ERR_UNSUPPORTED, "the FP8-cache decode runs on the tcgen05 kernel: H a multiple of 64 (H = %d)",
                 H);
-  nvmla_decode_options o{NVMLA_IMPL_TCGEN05, opts ? opts->num_splits : 0};
+  nvmla_decode_options o{NVMLA_IMPL_TCGEN05, opts ? opts->num_splits : 0, 0};
   int splits = 1;
   if ((s = pick_splits(NVMLA_IMPL_TCGEN05, &o, T, H, topk, workspace_bytes, workspace, &splits)) != NVMLA_OK) return s;
   RowSelect sel{topk_idx, block_table, q_seq_idx, seq_lens, num_pages * NVMLA_PAGE_TOKENS, topk, max_pages_per_seq,
                 num_seqs, NVMLA_PAGE_TOKENS};
   return counted(launch_decode_tc(2, q_latent, q_rope, cache, sel, nullptr, T, H, topk, sm_scale, out, lse, workspace,
-                                  splits, err_word, reinterpret_cast<cudaStream_t>(stream)),
+                                  splits, err_word, reinterpret_cast<cudaStream_t>(stream), 0, force_timeout(opts)),
                  1, "sparse_mla_decode_fp8cache launch");
 }
 
@@ -437,7 +456,8 @@ nvmla_status sparse_mla_decode_fp8rows(const void* q_latent, const void* q_rope,
   if (!fp8_rows || !row_idx) return fail(NVMLA_ERR_INVALID_ARG, "null fp8_rows/row_idx");
   if (!aligned(fp8_rows, 16) || !aligned(row_idx, 4)) return fail(NVMLA_ERR_INVALID_ARG, "fp8_rows must be 16-byte aligned");
   if (err_word && !aligned(err_word, 4)) return fail(NVMLA_ERR_INVALID_ARG, "err_word must be 4-byte aligned");
-  if (opts && (opts->impl < 0 || opts->impl > NVMLA_IMPL_TCGEN05 || opts->num_splits < 0))
+  if (opts && (opts->impl < 0 || opts->impl > NVMLA_IMPL_TCGEN05 || opts->num_splits < 0 ||
+               (opts->debug_flags & ~NVMLA_DEBUG_FORCE_WAIT_TIMEOUT) != 0))
     return fail(NVMLA_ERR_INVALID_ARG, "bad options");
   RowSelect sel{};
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -448,7 +468,7 @@ nvmla_status sparse_mla_decode_fp8rows(const void* q_latent, const void* q_rope,
   if ((s = pick_splits(impl, opts, T, H, topk, workspace_bytes, workspace, &splits)) != NVMLA_OK) return s;
   if (impl == NVMLA_IMPL_TCGEN05) {
     return counted(launch_decode_tc(1, q_latent, q_rope, fp8_rows, sel, row_idx, T, H, topk, sm_scale, out, lse,
-                                    workspace, splits, err_word, st),
+                                    workspace, splits, err_word, st, 0, 0),
                    splits > 1 ? 2 : 1, "sparse_mla_decode_fp8rows (tcgen05) launch");
   }
   return counted(launch_decode_mma(1, q_latent, q_rope, fp8_rows, sel, row_idx, T, H, topk, sm_scale, out, lse,

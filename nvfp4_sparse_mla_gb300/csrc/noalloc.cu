@@ -35,7 +35,10 @@ void* g_scratch[kMaxDevices] = {nullptr};
 std::mutex g_scratch_mu;
 
 // Device address of the scratch on the current device, looked up once per
-// device.
+// device and kept: it belongs to the device's primary context, so a
+// cudaDeviceReset (which destroys that context and unloads this module)
+// leaves a stale address; the header tells callers not to call again after
+// one.
 cudaError_t scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

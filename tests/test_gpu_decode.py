@@ -261,3 +261,31 @@ def test_large_score_range_rescales(lib, cuda):
                                              w.sm_scale, q_seq_idx=d["q_seq_idx"], seq_lens=d["seq_lens"],
                                              impl=impl, num_splits=splits)
             parity.assert_close(out, lse, ro, rl, f"wide scores impl={impl} splits={splits}")
+
+
+@pytest.mark.parametrize("splits", [1, 4])
+def test_forced_wait_timeout_reports_and_recovers(lib, cuda, splits):
+    """The tcgen05 kernel's bounded-wait abort path, made to run by the test
+    hook that has the MMA thread's wait for P^T give up at once: the call
+    completes (every CTA drains its MMAs, frees TMEM and meets the cluster
+    barriers), err_word carries NVMLA_ERRW_WAIT_TIMEOUT, and the next normal
+    call on the same stream matches the oracle."""
+    w = workloads.decode_point(seed=13, T=3, ctx=20_000)
+    cache = parity.device_cache(lib, w, cuda)
+    ref_cache = parity.oracle_cache(w)
+    ro, rl, _ = parity.oracle_decode(w, ref_cache)
+    d = parity.device_inputs(w, cuda)
+    err = torch.zeros(2, dtype=torch.int32, device=cuda)
+    lib.sparse_mla_decode(d["q_latent"], d["q_rope"], cache, d["block_table"], d["topk_idx"], w.sm_scale,
+                          q_seq_idx=d["q_seq_idx"], seq_lens=d["seq_lens"], err_word=err, impl=lib.IMPL_TCGEN05,
+                          num_splits=splits, debug_flags=lib.DEBUG_FORCE_WAIT_TIMEOUT)
+    torch.cuda.synchronize()
+    flags, count = err.cpu().tolist()
+    assert flags == 8 and count >= 1, (flags, count)  # NVMLA_ERRW_WAIT_TIMEOUT only
+    err.zero_()
+    out, lse = lib.sparse_mla_decode(d["q_latent"], d["q_rope"], cache, d["block_table"], d["topk_idx"], w.sm_scale,
+                                     q_seq_idx=d["q_seq_idx"], seq_lens=d["seq_lens"], err_word=err,
+                                     impl=lib.IMPL_TCGEN05, num_splits=splits)
+    torch.cuda.synchronize()
+    assert err.cpu().tolist() == [0, 0]
+    parity.assert_close(out, lse, ro, rl, f"after a forced timeout, splits={splits}")

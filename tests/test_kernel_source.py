@@ -30,10 +30,10 @@ def test_barrier_slots_are_distinct_and_dense():
     body = re.search(r"enum Bar \{(.*?)\};", src, re.S).group(1)
     values = {n: int(v) for n, v in re.findall(r"(kBar\w+|kNumBars)\s*=\s*(\d+)", body)}
     n_bars = values.pop("kNumBars")
-    # kBarLastPV + j for j < 4 (one per PV block of the last tile)
+    # kBarPV + j for j < 4 (one per PV block of 128 value dims)
     width = {n: 1 for n in values}
-    width["kBarLastPV"] = 4
-    assert re.search(r"for \(int j = 0; j < 4; \+\+j\) mbar_init\(bar\(kBarLastPV \+ j\)", src)
+    width["kBarPV"] = 4
+    assert re.search(r"for \(int j = 0; j < 4; \+\+j\) mbar_init\(bar\(kBarPV \+ j\)", src)
     slots = sorted(s for n, v in values.items() for s in range(v, v + width[n]))
     assert slots == list(range(n_bars)), slots
 

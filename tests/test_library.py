@@ -111,14 +111,10 @@ def test_default_split_counts_follow_the_wave_cost_model(lib):
     # Without a device the library assumes 152 SMs holding 152 / S clusters
     # of S CTAs (S <= 8). Cost of S: waves * (19 + 5 * ceil(16 / S)) us, the
     # cheapest S, then the fewest splits with the same tiles per CTA. The
-    # split count shows in the workspace: T * (H / 64) * S partials of
-    # 64 x 512 fp16 values plus 64 (m, l) pairs (none for S = 1).
-    per = 64 * 512 * 2 + 64 * 2 * 4
-
+    # kernel takes no workspace: its partials stay in shared memory.
     def splits(T, H=64):
-        n = lib.sparse_mla_decode_workspace_size(T, H, 2048, impl=lib.IMPL_TCGEN05)
-        assert n % (T * (H // 64) * per) == 0
-        return max(1, n // (T * (H // 64) * per))
+        assert lib.sparse_mla_decode_workspace_size(T, H, 2048, impl=lib.IMPL_TCGEN05) == 0
+        return lib.sparse_mla_decode_splits(T, H, 2048, impl=lib.IMPL_TCGEN05)
 
     assert splits(1) == 8      # one wave: 19 + 10
     assert splits(15) == 8     # 15 clusters of 8 fit (19 resident)

@@ -4,8 +4,10 @@ keeps its split partials in the library's own device scratch.
 It must give the same bits as sparse_mla_decode handed a workspace of the
 default size (same kernels, same split count), on two calls in a row: the
 second call finds the first call's partials in the scratch and must not
-depend on them. The file name sorts last so that it also runs after every
-other GPU test in the process."""
+depend on them. The tcgen05 kernel (head counts that are multiples of 64)
+combines its splits in shared memory and needs no scratch; the mma.sync
+kernel (the other head counts) keeps fp32 partials there. The file name sorts
+last so that it also runs after every other GPU test in the process."""
 import ctypes
 
 import pytest
@@ -15,15 +17,38 @@ import parity
 from nvfp4_sparse_mla_gb300 import workloads
 
 SCRATCH_BYTES = 16 << 20
+SMS = 152  # the no-device model and a GB300
 
 
-def test_scratch_size_and_fits(lib):
+def _bound(T, H, sms=SMS):
+    """The header's bound on the scratch a call needs: the mma.sync kernel
+    keeps T * S * H * (512 + 2) fp32 values, and its split count S gives
+    T * S <= floor(sms / ceil(H / 64)); head counts that are multiples of 64
+    need none."""
+    if H % 64 == 0:
+        return 0
+    return (sms // ((H + 63) // 64)) * H * 514 * 4
+
+
+def test_scratch_size(lib):
     assert lib.sparse_mla_decode_noalloc_max_scratch() == SCRATCH_BYTES
-    # the 15-token, 64-head, top-2048 decode point (tcgen05 kernel) and the
-    # same with 48 heads (mma.sync kernel) use the scratch and fit
-    for H in (64, 48):
-        need = lib.sparse_mla_decode_workspace_size(15, H, 2048)
-        assert 0 < need <= SCRATCH_BYTES
+
+
+@pytest.mark.skipif(torch.cuda.is_available() and torch.cuda.get_device_properties(0).multi_processor_count != SMS,
+                    reason="the bound is stated for 152 SMs")
+def test_every_shape_within_the_stated_bound(lib):
+    """Host-only sweep of every token count at every head count (top-2048):
+    the scratch a call needs never exceeds the header's bound, which fits
+    the 16 MiB scratch for every head count but 112."""
+    for H in range(16, 129, 16):
+        b = _bound(64, H)
+        assert (b <= SCRATCH_BYTES) == (H != 112), H
+        worst = 0
+        for T in range(1, 65536):
+            need = lib.sparse_mla_decode_workspace_size(T, H, 2048)
+            assert need <= b, (T, H, need, b)
+            worst = max(worst, need)
+        assert worst == 0 if H % 64 == 0 else worst > 0, H
 
 
 def test_rejects_shapes_beyond_the_scratch(lib):
@@ -71,14 +96,26 @@ def _noalloc(lib, w, cache, d, out, lse, err):
                                          err_word=err)
 
 
+def _workload(name):
+    if name == "h48_near_limit":
+        # 15 tokens x 48 heads: the mma.sync kernel with 10 splits, 14.8 MB
+        # of the 16 MiB scratch
+        return workloads.decode_point(seed=21, T=15, H=48, ctx=20_000)
+    return workloads.make(name)
+
+
 @pytest.mark.gpu
-@pytest.mark.parametrize("name", ["decode_point", "tiny"])
+@pytest.mark.parametrize("name", ["decode_point", "tiny", "h48_near_limit"])
 def test_two_calls_match_sparse_mla_decode(lib, cuda, name):
-    """decode_point runs the tcgen05 kernel with 8 splits (fp16 partials,
-    combined inside the kernel) and tiny (16 heads) the mma.sync kernel with
-    its fp32 partials and merge kernel: both go through the scratch."""
-    w = workloads.make(name)
-    assert lib.sparse_mla_decode_workspace_size(w.T, w.H, w.topk_idx.shape[1]) > 0
+    """decode_point runs the tcgen05 kernel with 8 splits combined in shared
+    memory (no scratch); tiny (16 heads) and h48_near_limit (48 heads) run the
+    mma.sync kernel with fp32 partials in the scratch and its merge kernel."""
+    w = _workload(name)
+    need = lib.sparse_mla_decode_workspace_size(w.T, w.H, w.topk_idx.shape[1])
+    assert (need > 0) == (w.H % 64 != 0)
+    assert need <= SCRATCH_BYTES
+    if name == "h48_near_limit":
+        assert need > (14 << 20)
     cache = parity.device_cache(lib, w, cuda)
     a, b = _inputs(w, cuda)
     ref_a = _reference(lib, w, cache, a)
@@ -89,13 +126,17 @@ def test_two_calls_match_sparse_mla_decode(lib, cuda, name):
     # warm-up: loads the library's code and looks up the scratch
     _noalloc(lib, w, cache, a, outs[2], lses[2], err)
     torch.cuda.synchronize()
+    # nothing else allocates between the two readings: this process's torch
+    # allocator (memory_allocated) and the device (free bytes) must not move
+    allocated = torch.cuda.memory_allocated(cuda)
     free_before = torch.cuda.mem_get_info(cuda)[0]
     launches = lib.launch_count()
     _noalloc(lib, w, cache, a, outs[0], lses[0], err)
     _noalloc(lib, w, cache, b, outs[1], lses[1], err)
     torch.cuda.synchronize()
+    assert torch.cuda.memory_allocated(cuda) == allocated, "the calls allocated through torch"
     assert torch.cuda.mem_get_info(cuda)[0] == free_before, "the calls changed the device's free memory"
-    assert lib.launch_count() - launches == (4 if name == "tiny" else 2)  # per call: decode (+ merge)
+    assert lib.launch_count() - launches == (2 if w.H % 64 == 0 else 4)  # per call: decode (+ merge)
     assert err.tolist() == [0, 0]
     assert torch.equal(outs[0], ref_a[0]) and torch.equal(lses[0], ref_a[1]), "first call differs"
     assert torch.equal(outs[1], ref_b[0]) and torch.equal(lses[1], ref_b[1]), "second call differs"
