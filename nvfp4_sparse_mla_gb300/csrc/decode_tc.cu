@@ -84,9 +84,22 @@ __device__ unsigned long long nvmla_tc_trace[kTraceCtas][kTracePoints];
       nvmla_tc_trace[cta_][(id)] = t_;                                                              \
     }                                                                                               \
   } while (0)
+// the same, once the 32-bit value v is available
+#define NVMLA_TRACE_AFTER(id, v)                                                                    \
+  do {                                                                                              \
+    const int cta_ = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);                 \
+    if (cta_ < kTraceCtas) {                                                                        \
+      unsigned long long t_;                                                                        \
+      asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t_) : "r"(v));                               \
+      nvmla_tc_trace[cta_][(id)] = t_;                                                              \
+    }                                                                                               \
+  } while (0)
 #else
 #define NVMLA_TRACE_POINT(id) \
   do {                        \
+  } while (0)
+#define NVMLA_TRACE_AFTER(id, v) \
+  do {                           \
   } while (0)
 #endif
 
@@ -124,17 +137,25 @@ enum Bar {
   kBarP = 3,       // P^T written, O^T rescaled if needed (16 worker warps)
   kBarPV = 4,      // 4: PV block j done, its two latent chunks reusable (commit)
   kBarDrain = 8,   // every MMA finished (commit)
-  kNumBars = 9
+  kBarRows0 = 9,   // NVFP4: the first tile's rows have landed (TMA; one arrival per row)
+  kNumBars = 10
 };
 constexpr int kOffMisc = kOffBar + kNumBars * 8;      // tmem base, abort flag
 constexpr int kSmemBytes = kOffMisc + 16;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kOffKV % 1024 == 0 && kOffP % 1024 == 0, "swizzled operands need 1 KB alignment");
-static_assert(kQBytes <= 8 * kChunkBytes, "the raw query block lands in the latent tile");
+static_assert(kQBytes == 9 * 8192, "the raw query block lands in the Q^T space and is converted in place");
+// NVFP4: the first tile's 128 rows land by TMA in the latent tile's space,
+// 368 bytes apart (23 units of 16 bytes: the rows of 32 consecutive lanes
+// fall into distinct banks)
+constexpr int kRawPitch = 368;
+constexpr int kOffRaw0 = kOffKV;
+static_assert(kOffRaw0 + kTile * kRawPitch <= kOffKV + 8 * kChunkBytes, "first-tile rows fit the latent tile");
 static_assert(kOffMl % 16 == 0, "(m, l) block alignment");
 
-// value dims [dim_lo(r), dim_lo(r + 1)) are combined by CTA r of S
-__host__ __device__ constexpr int dim_lo(int r, int S) { return (r * kLatent) / S; }
+// value dims [dim_lo(r), dim_lo(r + 1)) are combined by CTA r of S: whole
+// groups of 8 dims, so that each CTA's share of a head row is 16-byte units
+__host__ __device__ constexpr int dim_lo(int r, int S) { return 8 * ((r * (kLatent / 8)) / S); }
 
 struct Params {
   const __nv_bfloat16* q_latent;
@@ -563,13 +584,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
   // latent tile's space; the workers convert it once it has landed
   if (tid == 0) {
     mbar_init(bar(kBarQ), 1);
+    mbar_init(bar(kBarRows0), kTile);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_async_smem();
     mbar_arrive_expect_tx(bar(kBarQ), kQBytes);
     const int64_t qh0 = static_cast<int64_t>(t) * p.H + h0;
-    bulk_load(sbase + kOffKV, p.q_latent + qh0 * kLatent, kHeads * kLatent * 2, bar(kBarQ));
-    bulk_load(sbase + kOffKV + kHeads * kLatent * 2, p.q_rope + qh0 * kRope, kHeads * kRope * 2, bar(kBarQ));
+    bulk_load(sbase + kOffQ, p.q_latent + qh0 * kLatent, kHeads * kLatent * 2, bar(kBarQ));
+    bulk_load(sbase + kOffQ + kHeads * kLatent * 2, p.q_rope + qh0 * kRope, kHeads * kRope * 2, bar(kBarQ));
   }
+  // the first tile's row barrier is initialised before any thread arrives on it
+  __syncthreads();
 
   const bool is_worker = tid < kWorkers;
   const int quad = warp & 3, qu = (warp >> 2) & 3;  // workers: TMEM lane quadrant, row quarter
@@ -627,8 +651,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
   auto row_of = [&](int32_t slot) { return p.cache + cache_row_offset(slot, p.sel.page_rows, kRB); };
   int32_t page0 = 0;
   int32_t pagel[kLaterPer];
+  if (tid == 0) NVMLA_TRACE_AFTER(25, pos0);
   if (is_worker) {
     page0 = page_of(pos0);
+    if (tid == 0) NVMLA_TRACE_AFTER(26, page0);
 #pragma unroll
     for (int m = 0; m < kLaterPer; ++m) pagel[m] = (1 + qu + 4 * m < ntiles) ? page_of(posl[m]) : 0;
   }
@@ -637,16 +663,31 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
     const int64_t L = ldg_nc_s32(p.sel.seq_lens + seq);
     limit = L < limit ? L : limit;
   }
+  if (tid == 0) NVMLA_TRACE_AFTER(27, static_cast<int32_t>(limit));
 
-  // ---- level 3: this thread's quarter of its first-tile row, into
-  // registers; the later tiles' slots into shared memory, their rows
-  // prefetched into L2
+  // ---- level 3: the first tile's rows (NVFP4: one TMA bulk copy per row
+  // into shared memory, issued by the row's quarter-0 thread; FP8: this
+  // thread's quarter of its row into registers); the later tiles' slots into
+  // shared memory, their rows prefetched into L2
   Quarter<FMT> raw;
   int32_t slot0 = -1;
   if (is_worker) {
     const bool mine = ntiles > 0 && kbeg + r < kend;
     const int32_t sspec = mine ? phys_slot(pos0, page0) : -1;
-    if (sspec >= 0) load_quarter<FMT>(raw, row_of(sspec), qu);
+    if constexpr (FMT == kFmtNvfp4) {
+      if (qu == 0) {
+        // the barrier must see this thread's arrival before the copy's bytes
+        if (sspec >= 0) {
+          mbar_arrive_expect_tx(bar(kBarRows0), kRowBytes);
+          bulk_load(sbase + kOffRaw0 + r * kRawPitch, row_of(sspec), kRowBytes, bar(kBarRows0));
+        } else {
+          mbar_arrive(bar(kBarRows0));
+        }
+      }
+    } else {
+      if (sspec >= 0) load_quarter<FMT>(raw, row_of(sspec), qu);
+    }
+    if (tid == 0) NVMLA_TRACE_POINT(28);
     if (mine) slot0 = classify(pos0, page0, limit, report && qu == 0);
     if (qu == 0) slots[r] = slot0;
 #pragma unroll
@@ -691,23 +732,31 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
     // ------------------------------------------------------------ workers
     // query block -> fp16 Q^T, K-major 128B-swizzled (4608 pieces of 16
     // bytes), out of the latent tile's space
-    ok = ok && wait_bar_warp(bar(kBarQ), 0, abort_flag, p.err_word);
-    if (tid == 0) NVMLA_TRACE_POINT(2);
-    if (ok) {
-      const uint8_t* qraw = smem + kOffKV;
-#pragma unroll 3
-      for (int it = tid; it < kHeads * 72; it += kWorkers) {
-        const int h = it / 72, j = it - (it / 72) * 72, c = j >> 3, q = j & 7;
-        const uint4 v = *reinterpret_cast<const uint4*>(
-            qraw + (j < 64 ? h * (kLatent * 2) + 16 * j : kHeads * kLatent * 2 + h * (kRope * 2) + 16 * (j - 64)));
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        uint32_t o[4];
+    if constexpr (FMT == kFmtNvfp4) {
+      // this thread's quarter of its first-tile row, out of shared memory
+      ok = ok && wait_bar_warp(bar(kBarRows0), 0, abort_flag, p.err_word);
+      if (ok) {
+        const uint8_t* row = smem + kOffRaw0 + r * kRawPitch;
+        const uint4 c0 = *reinterpret_cast<const uint4*>(row + 64 * qu);
+        const uint4 c1 = *reinterpret_cast<const uint4*>(row + 64 * qu + 16);
+        const uint4 c2 = *reinterpret_cast<const uint4*>(row + 64 * qu + 32);
+        const uint4 c3 = *reinterpret_cast<const uint4*>(row + 64 * qu + 48);
+        const uint2 sc = *reinterpret_cast<const uint2*>(row + kScaleOff + 8 * qu);
+        const uint4 rr = *reinterpret_cast<const uint4*>(row + kRopeOff + 16 * qu);
+        const uint32_t cw[16] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w,
+                                 c2.x, c2.y, c2.z, c2.w, c3.x, c3.y, c3.z, c3.w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) o[e] = pack_f16x2(bf16_bits_to_f32(w[e] & 0xffffu), bf16_bits_to_f32(w[e] >> 16));
-        *reinterpret_cast<uint4*>(smem + kOffQ + c * 8192 + swz(h, q)) = make_uint4(o[0], o[1], o[2], o[3]);
+        for (int k = 0; k < 16; ++k) raw.c[k] = cw[k];
+        raw.sc[0] = sc.x;
+        raw.sc[1] = sc.y;
+        raw.rr[0] = rr.x;
+        raw.rr[1] = rr.y;
+        raw.rr[2] = rr.z;
+        raw.rr[3] = rr.w;
       }
     }
-    // every worker is done with the raw query block before the tile reuses it
+    if (tid == 0) NVMLA_TRACE_POINT(29);
+    // every worker holds its first-tile row before the tile's space is written
     ok = !workers_sync_or(!ok);
     if (tid == 0) NVMLA_TRACE_POINT(3);
 
@@ -717,31 +766,73 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
     uint8_t* chunk0 = smem + kOffKV + (2 * qu) * kChunkBytes;
     const uint32_t rope_col = tmem + lane_base + kColR + 8 * qu;
     const int hb = 16 * qu;  // first head of this thread's softmax share
+    // this thread's part of a tile: latent chunks 2qu, 2qu + 1 of row r into
+    // the latent tile, its RoPE dims into TMEM
+    auto unpack = [&](bool valid) {
+      store_chunk<FMT>(raw, 0, valid, chunk0, r);
+      store_chunk<FMT>(raw, 1, valid, chunk0 + kChunkBytes, r);
+      tc_fence_after();
+      store_rope<FMT>(raw, valid, rope_col);
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+    };
+    // ---- the first tile is unpacked while the query block is still landing
+    if (ok && ntiles > 0) unpack(slots[r] >= 0);
+    if (tid == 0) NVMLA_TRACE_POINT(30);
+    // ---- the query block -> fp16 Q^T, K-major 128B-swizzled, in place: this
+    // thread's 9 pieces of 16 bytes into registers, a barrier, then converted
+    // to their swizzled places
+    {
+      bool okq = ok && wait_bar_warp(bar(kBarQ), 0, abort_flag, p.err_word);
+      if (tid == 0) NVMLA_TRACE_POINT(2);
+      uint4 qv[9];
+      if (okq) {
+#pragma unroll
+        for (int m = 0; m < 9; ++m) {
+          const int it = tid + kWorkers * m, h = it / 72, j = it - (it / 72) * 72;
+          qv[m] = *reinterpret_cast<const uint4*>(
+              smem + kOffQ +
+              (j < 64 ? h * (kLatent * 2) + 16 * j : kHeads * kLatent * 2 + h * (kRope * 2) + 16 * (j - 64)));
+        }
+      }
+      okq = !workers_sync_or(!okq);
+      if (okq) {
+#pragma unroll
+        for (int m = 0; m < 9; ++m) {
+          const int it = tid + kWorkers * m, h = it / 72, j = it - (it / 72) * 72, c = j >> 3, q = j & 7;
+          const uint32_t w[4] = {qv[m].x, qv[m].y, qv[m].z, qv[m].w};
+          uint32_t o[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) o[e] = pack_f16x2(bf16_bits_to_f32(w[e] & 0xffffu), bf16_bits_to_f32(w[e] >> 16));
+          *reinterpret_cast<uint4*>(smem + kOffQ + c * 8192 + swz(h, q)) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+      ok = okq;
+      if (tid == 0) NVMLA_TRACE_POINT(3);
+    }
+    if (ok && ntiles > 0) {
+      fence_async_smem();
+      tc_fence_before();
+      warp_arrive(bar(kBarKV), lane);
+    }
     for (int i = 0; i < ntiles && ok; ++i) {
       const bool valid = slots[i * kTile + r] >= 0;
       // ---- unpack tile i: chunks 2qu, 2qu + 1 once PV block qu of the
       // previous tile is done; the RoPE K once QK of the previous tile is
       // done (waited for below, in its softmax)
       bool okw = true;
-      if (i >= 1) okw = wait_bar_warp(bar(kBarPV + qu), (i - 1) & 1, abort_flag, p.err_word);
-      if (okw) {
-        store_chunk<FMT>(raw, 0, valid, chunk0, r);
-        store_chunk<FMT>(raw, 1, valid, chunk0 + kChunkBytes, r);
-        tc_fence_after();
-        store_rope<FMT>(raw, valid, rope_col);
-        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-        fence_async_smem();
-        tc_fence_before();
-        warp_arrive(bar(kBarKV), lane);
+      if (i >= 1) {
+        okw = wait_bar_warp(bar(kBarPV + qu), (i - 1) & 1, abort_flag, p.err_word);
+        if (okw) {
+          unpack(valid);
+          fence_async_smem();
+          tc_fence_before();
+          warp_arrive(bar(kBarKV), lane);
+        }
       }
       if (tid == 0 && i < 2) NVMLA_TRACE_POINT(4 + 8 * i);
-      // ---- the next tile's row into the same registers
-      if (i + 1 < ntiles) {
-        const int32_t ns = slots[(i + 1) * kTile + r];
-        if (ns >= 0) load_quarter<FMT>(raw, row_of(ns), qu);
-      }
       // ---- softmax of tile i
       if (okw) okw = wait_bar_warp(bar(kBarS), i & 1, abort_flag, p.err_word);
+      if (tid == 0 && i < 2) NVMLA_TRACE_POINT(11 + 8 * i);
       if (workers_sync_or(!okw)) {
         ok = false;
         break;
@@ -843,6 +934,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
       fence_async_smem();
       tc_fence_before();
       warp_arrive(bar(kBarP), lane);
+      // ---- the next tile's row into the same registers
+      if (i + 1 < ntiles) {
+        const int32_t ns = slots[(i + 1) * kTile + r];
+        if (ns >= 0) load_quarter<FMT>(raw, row_of(ns), qu);
+      }
       if (tid == 0 && i < 2) NVMLA_TRACE_POINT(6 + 8 * i);
     }
     // ------------------------------------------------------------ row sums
@@ -947,6 +1043,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
         mma_chunk_qk<7 * 1024, 7 * 512>(tmem + kColS, a_kv, b_q, idesc_qk, 1);
         mma_chunk_qk_tmem<8 * 512>(tmem + kColS, tmem + kColR, b_q, idesc_qk);
         mma_commit(bar(kBarS));
+        if (i < 2) NVMLA_TRACE_POINT(9 + 8 * i);
         mok = p.force_p_timeout ? give_up(abort_flag, p.err_word)
                                 : wait_bar(bar(kBarP), i & 1, abort_flag, p.err_word, p_limit);
         if (!mok) break;
@@ -964,6 +1061,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
         mma_commit(bar(kBarPV + 2));
         mma_block_pv<3 * 2048>(tmem + kColO + 3 * 64, a_v, b_p, idesc_pv, acc);
         mma_commit(bar(kBarPV + 3));
+        if (i < 2) NVMLA_TRACE_POINT(10 + 8 * i);
       }
       // every MMA this thread issued has finished once this commit lands
       mma_commit(bar(kBarDrain));
@@ -978,8 +1076,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
   }
-  // the query block's copy has landed before this CTA's shared memory can go
-  if (tid == 0) wait_bar_drain(bar(kBarQ), 0);
+  // the query block's and the first tile's copies have landed before this
+  // CTA's shared memory can go
+  if (tid == 0) {
+    wait_bar_drain(bar(kBarQ), 0);
+    if (FMT == kFmtNvfp4) wait_bar_drain(bar(kBarRows0), 0);
+  }
   if (S > 1) {
     // release / acquire at cluster scope: every CTA's staged partial and
     // (m, l) are visible to every CTA of the cluster
@@ -1021,19 +1123,26 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
     }
     __syncthreads();
     if (tid == 0) NVMLA_TRACE_POINT(23);
-    // item = (dim d, head group v of 8 heads): lanes take consecutive dims;
-    // each split's 16 bytes come straight from its CTA's shared memory
+    // item = (dim d, 16-byte unit u of its staged row): eight consecutive
+    // lanes read one dim row, so a warp reads 512 contiguous bytes of a
+    // peer's shared memory at a time; unit u holds heads 8 (u ^ (d & 7))..+7.
+    // The sums go, transposed, to a [64 heads][D dims] bf16 buffer in the
+    // query block's space (free since the last QK): 8-dim unit c of head h
+    // at unit c ^ (h >> 3) of its row, so that the eight head groups a warp
+    // writes at once fall into different banks.
+    const int pitch = (D + 63) / 64 * 64;  // bf16 elements per head row of the buffer
+    __nv_bfloat16* tb = reinterpret_cast<__nv_bfloat16*>(smem + kOffQ);
     for (int it = tid; it < D * 8; it += kThreads) {
-      const int v = it / D, d = d0 + (it - v * D);
-      const uint32_t off = sbase + kOffKV + d * 128 + ((v ^ (d & 7)) << 4);
+      const int dd = it >> 3, u = it & 7, d = d0 + dd, v = u ^ (d & 7);
+      const uint32_t off = sbase + kOffKV + d * 128 + u * 16;
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      for (int s0 = 0; s0 < S; s0 += 4) {
-        uint4 part[4];
+      for (int s0 = 0; s0 < S; s0 += 8) {
+        uint4 part[8];
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
+        for (int k = 0; k < 8; ++k)
           part[k] = (s0 + k < S) ? ld_cluster_v4(map_rank(off, static_cast<uint32_t>(s0 + k))) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < 8; ++k) {
           if (s0 + k >= S) break;
           const uint32_t w[4] = {part[k].x, part[k].y, part[k].z, part[k].w};
           const float4 c0 = *reinterpret_cast<const float4*>(coef + (s0 + k) * kHeads + 8 * v);
@@ -1047,10 +1156,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
           }
         }
       }
-      // straight to out: the lanes of a warp write consecutive dims of a head
-      __nv_bfloat16* o = p.out + (static_cast<int64_t>(t) * p.H + h0 + 8 * v) * kLatent + d;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) o[e * kLatent] = __float2bfloat16_rn(acc[e]);
+      for (int e = 0; e < 8; ++e) tb[(8 * v + e) * pitch + 8 * ((dd >> 3) ^ v) + (dd & 7)] = __float2bfloat16_rn(acc[e]);
+    }
+    __syncthreads();
+    // out rows of this CTA's dims, 16 bytes a thread: a warp writes whole
+    // 128-byte runs of a head row
+    const int upr = D / 8;  // 16-byte units per head row
+    for (int it = tid; it < kHeads * upr; it += kThreads) {
+      const int h = it / upr, c = it - h * upr;
+      *reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(t) * p.H + h0 + h) * kLatent + d0 + 8 * c) =
+          *reinterpret_cast<const uint4*>(tb + h * pitch + 8 * (c ^ (h >> 3)));
     }
     // no CTA leaves while another may still read its shared memory
     cluster_sync_all();
