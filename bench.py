@@ -53,6 +53,7 @@ def parse():
     ap.add_argument("--no-layered", action="store_true")
     ap.add_argument("--no-topk", action="store_true")
     ap.add_argument("--no-fp8", action="store_true")
+    ap.add_argument("--no-configs", action="store_true")
     return ap.parse_args()
 
 
@@ -96,6 +97,90 @@ def algorithmic(w):
     out = T * H * 512 * 2 + T * H * 4
     flops = valid * H * (2 * 576 + 2 * 512)
     return {"bytes": rows + q + idx + bt + out, "row_bytes": rows, "flops": flops, "valid_slots": valid}
+
+
+def graph_us(fn, reps=5):
+    """Median device time of one replay of a CUDA graph that runs `fn` (which
+    enqueues on the current stream), in microseconds."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cap):
+        fn()  # warm-up outside the capture (library set-up, allocator)
+    torch.cuda.current_stream().wait_stream(cap)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        fn()
+    g.replay()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        b.synchronize()
+        ts.append(a.elapsed_time(b) * 1e3)
+    del g
+    return statistics.median(ts)
+
+
+def kernel_only_us(call, flush, n=20):
+    """Device time of `call` alone: a CUDA graph of n x (L2 flush, call) less
+    a graph of the n flushes, per call (cold L2); and a graph of n calls back
+    to back, per call (warm L2). Graph replay keeps the host's launch latency
+    out of both."""
+    def flushed():
+        for k in range(n):
+            flush.fill_(float(k))
+            call()
+
+    def flushes():
+        for k in range(n):
+            flush.fill_(float(k))
+
+    def warm():
+        for _ in range(n):
+            call()
+
+    cold = (graph_us(flushed) - graph_us(flushes)) / n
+    return {"cold_l2_us": cold, "warm_l2_us": graph_us(warm) / n, "calls_per_graph": n,
+            "how": "CUDA graph of n x (256 MiB L2 flush, call) minus a graph of the n flushes, per call; "
+                   "warm: a graph of n calls back to back, per call"}
+
+
+def event_us(call, flush, steps, before=None):
+    """Mean event time of `call` per step, L2 flushed before every step, steps
+    queued behind a GPU sleep so that the events bracket device work only."""
+    import torch
+    evs = []
+    for k in range(steps):
+        if k % GROUP == 0:
+            torch.cuda._sleep(LEAD_CYCLES_PER_STEP * min(GROUP, steps - k))
+        flush.fill_(float(k))
+        if before is not None:
+            before()
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        e[0].record()
+        call()
+        e[1].record()
+        evs.append(e)
+    torch.cuda.synchronize()
+    return statistics.mean([e[0].elapsed_time(e[1]) for e in evs]) * 1e3
+
+
+def roofline_of(alg, us, pk):
+    """Achieved rate of one call against the bound that limits it."""
+    bw, tf = pk["hbm_gbs"], pk["bf16_tflops"]
+    t_bytes = alg["bytes"] / (bw * 1e9) * 1e6
+    t_flops = alg["flops"] / (tf * 1e12) * 1e6
+    if t_flops >= t_bytes:
+        ach = alg["flops"] / (us * 1e-6) / 1e12
+        return {"bound": "tensor", "achieved": ach, "peak": tf, "unit": "TFLOP/s", "frac": ach / tf,
+                "roofline_us": t_flops}
+    ach = alg["bytes"] / (us * 1e-6) / 1e9
+    return {"bound": "hbm", "achieved": ach, "peak": bw, "unit": "GB/s", "frac": ach / bw, "roofline_us": t_bytes}
 
 
 class ClockSampler:
@@ -236,9 +321,31 @@ def cpu_baseline(w, seconds: float):
         if el >= seconds:
             break
     threads = blas_threads()
-    return {"value": el / n * 1e6, "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"{n} whole decode calls of the workload (15 tokens x 2048 slots each), "
-                      f"numpy float64 with a {threads}-thread BLAS on {os.cpu_count()} host cores"}
+    res = {"value": el / n * 1e6, "unit": UNIT, "cores": threads, "kind": "oracle",
+           "sample": f"{n} whole decode calls of the workload (15 tokens x 2048 slots each), "
+                     f"numpy float64 with a {threads}-thread BLAS on {os.cpu_count()} host cores"}
+    # the same oracle on one host thread: a child process whose BLAS is held
+    # to one thread from the start
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = ("import sys, time; sys.path.insert(0, %r); import numpy as np; "
+            "from nvfp4_sparse_mla_gb300 import workloads; from oracle import attention as oatt; "
+            "from oracle import pack as opack; w = workloads.decode_point(); lat, rope, slots = w.all_written(); "
+            "cache = np.zeros((w.num_pages + 1, 64, 352), dtype=np.uint8); "
+            "opack.pack_into_cache(lat.double().numpy(), rope.double().numpy(), slots.numpy(), cache); "
+            "n, t0 = 0, time.perf_counter()\n"
+            "while True:\n"
+            "    oatt.sparse_mla_decode(w.q_latent, w.q_rope, cache, w.block_table, w.topk_idx, w.sm_scale, "
+            "w.q_seq_idx, w.seq_lens); n += 1; el = time.perf_counter() - t0\n"
+            "    if el >= %f: break\n"
+            "print(n, el / n * 1e6)") % (ROOT, seconds / 2)
+    try:
+        r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=300)
+        n1, us1 = r.stdout.split()
+        res["one_thread"] = {"value": float(us1), "unit": UNIT, "cores": 1,
+                             "sample": f"{n1} whole decode calls in a child process with a one-thread BLAS"}
+    except Exception as e:  # the all-cores figure stands on its own
+        res["one_thread"] = {"error": str(e)[:200]}
+    return res
 
 
 def blas_threads():
@@ -294,6 +401,93 @@ def run_reference(args, rank, world):
         "gpu_launches": 0,
     }
     print(json.dumps(line), flush=True)
+
+
+def config_line(name, args, flush, dev, pk, impl):
+    """One of the baseline's other workloads on the GPU: the decode call's
+    event time (L2 flushed before every call), its kernel-only times and its
+    roofline from the workload's actual valid slots; for write+read also the
+    pack of the 6,144-token chunk, the whole step (pack, then decode) and the
+    staged dequant-to-FP8 path timed the same way."""
+    import torch
+    import nvfp4_sparse_mla_gb300 as nvmla
+    from nvfp4_sparse_mla_gb300 import workloads
+    w = workloads.make(name)
+    alg = algorithmic(w)
+    cache = torch.zeros((w.num_pages, 64, 352), dtype=torch.uint8, device=dev)
+    nvmla.nvfp4_mla_pack(w.hist_latent.to(dev), w.hist_rope.to(dev), w.hist_slots.to(dev), cache)
+    nl, nr, ns = w.new_latent.to(dev), w.new_rope.to(dev), w.new_slots.to(dev)
+    if ns.numel():
+        nvmla.nvfp4_mla_pack(nl, nr, ns, cache)
+    ql, qr = w.q_latent.to(dev), w.q_rope.to(dev)
+    bt, tk = w.block_table.to(dev), w.topk_idx.to(dev)
+    qs, sl = w.q_seq_idx.to(dev), w.seq_lens.to(dev)
+    out = torch.empty((w.T, w.H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.T, w.H), dtype=torch.float32, device=dev)
+    ws_n = nvmla.sparse_mla_decode_workspace_size(w.T, w.H, w.topk, impl=impl)
+    ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=dev)
+
+    def decode():
+        nvmla.sparse_mla_decode(ql, qr, cache, bt, tk, w.sm_scale, out=out, lse=lse, q_seq_idx=qs, seq_lens=sl,
+                                workspace=ws, impl=impl)
+
+    for _ in range(3):
+        flush.fill_(1.0)
+        decode()
+    torch.cuda.synchronize()
+    steps = max(20, args.steps // 4)
+    us = event_us(decode, flush, steps)
+    ko = kernel_only_us(decode, flush)
+    line = {"workload": workloads.describe(w), "decode_us": us, "decode_kernel_only": ko,
+            "splits": nvmla.sparse_mla_decode_splits(w.T, w.H, w.topk, impl=impl),
+            "algorithmic_bytes": alg["bytes"], "algorithmic_flops": alg["flops"],
+            "roofline": roofline_of(alg, us, pk), "roofline_kernel": roofline_of(alg, ko["cold_l2_us"], pk)}
+    if name == "write_read":
+        def pack():
+            nvmla.nvfp4_mla_pack(nl, nr, ns, cache)
+
+        def step():
+            pack()
+            decode()
+
+        line["pack_us"] = event_us(pack, flush, steps)
+        line["step_us"] = event_us(step, flush, steps)
+        line["pack_tokens"] = int(ns.numel())
+        # the staged baseline over the same rows: dequantise to 576-byte FP8
+        # rows in GPU memory, then attend over them on the tcgen05 kernel (the
+        # buffer read as a paged FP8 cache, one block-table row per token)
+        buf = torch.empty((w.T, w.topk, 576), dtype=torch.uint8, device=dev)
+        ridx = torch.empty((w.T, w.topk), dtype=torch.int32, device=dev)
+        ppt = w.topk // 64
+        sbt = torch.arange(w.T * ppt, dtype=torch.int32, device=dev).view(w.T, ppt)
+        sqs = torch.arange(w.T, dtype=torch.int32, device=dev)
+        sview = buf.view(w.T * ppt, 64, 576)
+        fo, fl = torch.empty_like(out), torch.empty_like(lse)
+        ws2 = torch.empty(max(nvmla.sparse_mla_decode_workspace_size(w.T, w.H, w.topk), 16), dtype=torch.uint8,
+                          device=dev)
+
+        def dequant():
+            nvmla.nvfp4_stage_dequant_fp8(cache, bt, tk, qs, sl, fp8_rows=buf, row_idx=ridx)
+
+        def attend():
+            nvmla.sparse_mla_decode_fp8cache(ql, qr, sview, sbt, ridx, w.sm_scale, out=fo, lse=fl, q_seq_idx=sqs,
+                                             workspace=ws2)
+
+        def staged_step():
+            pack()
+            dequant()
+            attend()
+
+        dequant()
+        attend()
+        torch.cuda.synchronize()
+        st = {"dequant_us": event_us(dequant, flush, steps), "attend_us": event_us(attend, flush, steps, before=dequant),
+              "step_us": event_us(staged_step, flush, steps), "fp8_buffer_bytes": int(buf.numel())}
+        st["us_per_call"] = st["dequant_us"] + st["attend_us"]
+        line["staged"] = st
+        del buf, ridx
+    del cache
+    return line
 
 
 def main():
@@ -386,6 +580,8 @@ def main():
     dec_us = statistics.mean(dec_ms) * 1e3
     step_mean = statistics.mean(step_ms)
     dec_us, step_mean = max_over_ranks([dec_us, step_mean], world, dev)
+    # the decode call's device time without the event and launch overhead
+    dec_kernel = kernel_only_us(decode, flush)
 
     # ---------------- end to end through the public API with host buffers
     # Every per-step input (queries, index lists, the new tokens) lives in
@@ -666,6 +862,15 @@ def main():
     pack_us = statistics.mean([pk[2 * i].elapsed_time(pk[2 * i + 1]) for i in range(K)]) * 1e3
     pack_bytes = 6144 * (1152 + 352 + 4)
 
+    # ---------------- the other workloads the baseline names, same protocol
+    configs = None
+    if not args.no_configs:
+        configs = {}
+        pk_c, _ = peaks()
+        for cname in ("padded", "batched", "write_read"):
+            configs[cname] = config_line(cname, args, flush, dev, pk_c, impl)
+            torch.cuda.empty_cache()
+
     if rank != 0:
         return
     pk_peaks, peak_src = peaks()
@@ -699,7 +904,11 @@ def main():
                      "algorithmic_bytes": alg["bytes"], "algorithmic_flops": alg["flops"],
                      "effective_hbm_gbs": alg["bytes"] / (dec_us * 1e-6) / 1e9,
                      "kernel": kernel, "timed": "whole decode call (CUDA events on the launching stream)",
-                     "traffic": traffic},
+                     "traffic": traffic,
+                     "kernel_us": dec_kernel["cold_l2_us"],
+                     "frac_kernel": (alg["flops"] / (dec_kernel["cold_l2_us"] * 1e-6) / 1e12) / peak
+                     if bound == "tensor" else (alg["bytes"] / (dec_kernel["cold_l2_us"] * 1e-6) / 1e9) / peak},
+        "decode_kernel_only": dec_kernel,
         "decode_us": {"mean": dec_us, "median": statistics.median(dec_ms) * 1e3, "min": min(dec_ms) * 1e3},
         "pack_step_us": statistics.mean(pack_ms) * 1e3,
         "pack_chunk": {"tokens": 6144, "us_per_call": pack_us, "gbs": pack_bytes / (pack_us * 1e-6) / 1e9,
@@ -708,6 +917,7 @@ def main():
         "layered": layered,
         "topk_select": (dict(topk_sel, frac_hbm=topk_sel["gbs"] / bw) if topk_sel else None),
         "fp8_cache": fp8,
+        "configs": configs,
         "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "how": "per step: one host-to-device copy of every input from pinned memory, nvfp4_mla_pack, "
                        "sparse_mla_decode, one device-to-host copy of out and lse, replayed as a CUDA graph; "
