@@ -24,24 +24,31 @@
 // is V^T for PV. TMEM (512 columns): S^T in 0-63, O^T in 64-319 (block j =
 // dims 128j..128j+127), the tile's RoPE K in 320-351.
 //
-// Roles (17 warps, 120 registers a thread):
-//   warps 0-15  workers. Warp w owns TMEM lane quadrant w & 3 and quarter
-//               u = w >> 2: thread (row r = 32 (w & 3) + lane, quarter u)
-//               holds a quarter of cache row r -- latent dims 128u..128u+127
-//               (the code bytes and their 8 scales) and RoPE dims 16u..16u+15
-//               -- and writes them as fp16 (E2M1 x E4M3 is exact in fp16):
-//               the latent into chunks 2u, 2u+1 of the tile, the RoPE values
-//               into TMEM. The same thread then runs the softmax of row r for
-//               heads 16u..16u+15: S^T from TMEM, P^T to shared memory.
-//   warp 16     allocates TMEM; one thread issues every MMA: per tile the 36
-//               QK MMAs, then, once P^T is written, the 32 PV MMAs as four
-//               blocks of 128 value dims, each committed on its own so that
-//               the next tile's unpack refills that block's two chunks while
-//               the later blocks run.
+// Roles (16 warps, 128 registers a thread; a 17th warp would put five warps
+// on one SM sub-partition and cap every thread at 96 registers):
+//   every warp  warp w owns TMEM lane quadrant w & 3 and quarter u = w >> 2:
+//               thread (row r = 32 (w & 3) + lane, quarter u) holds a quarter
+//               of cache row r -- latent dims 128u..128u+127 (the code bytes
+//               and their 8 scales) and RoPE dims 16u..16u+15 -- and writes
+//               them as fp16 (E2M1 x E4M3 is exact in fp16): the latent into
+//               chunks 2u, 2u+1 of the tile, the RoPE values into TMEM. The
+//               same thread then runs the softmax of row r for heads
+//               16u..16u+15: S^T from TMEM, P^T to shared memory.
+//   warp 15     also allocates TMEM, and its lane 0 issues every MMA between
+//               its own steps: a tile's 36 QK MMAs right after the warp's
+//               part of the tile is written, the 32 PV MMAs (four blocks of
+//               128 value dims, each committed on its own so that the next
+//               tile's unpack refills that block's two chunks while the later
+//               blocks run) right after its share of P^T. The warp unpacks
+//               quarter 3, which waits for the last PV block in any case.
 //
-// Per tile the order is unpack -> QK -> softmax -> PV; the next tile's rows
-// are requested as soon as the current tile is unpacked (and were prefetched
-// to L2 at start-up), and its unpack overlaps the current PV.
+// Start-up: the slot-list entries, then the query block straight into
+// registers (converted to fp16 Q^T while the rows are on their way), then
+// the block-table entries; the first tile's rows come by one TMA bulk copy
+// each into the latent tile's space, the next tiles' rows are prefetched
+// into L2. Per tile the order is unpack -> QK -> softmax -> PV; a later
+// tile's rows are requested into registers after a softmax (NVFP4: two tiles
+// ahead), and a tile's unpack overlaps the previous PV block by block.
 //
 // Softmax: the running maximum of a head starts, on the first tile, at the
 // largest score of rows 0, 32, 64 and 96 and stays fixed while no score
@@ -57,7 +64,7 @@
 // writes bf16 out (rank 0 also writes lse). No global workspace is used.
 //
 // Every mbarrier wait is bounded: on timeout the CTA sets
-// NVMLA_ERRW_WAIT_TIMEOUT, the MMA thread drains its MMAs, and every thread
+// NVMLA_ERRW_WAIT_TIMEOUT, the MMA issuer drains its MMAs, and every thread
 // still takes part in the same cluster barriers, so that every CTA exits.
 #include "common.cuh"
 
@@ -94,11 +101,30 @@ __device__ unsigned long long nvmla_tc_trace[kTraceCtas][kTracePoints];
       nvmla_tc_trace[cta_][(id)] = t_;                                                              \
     }                                                                                               \
   } while (0)
+// a value instead of the time
+#define NVMLA_TRACE_VALUE(id, v)                                                                    \
+  do {                                                                                              \
+    const int cta_ = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);                 \
+    if (cta_ < kTraceCtas) nvmla_tc_trace[cta_][(id)] = (v);                                        \
+  } while (0)
+// tiles whose schedule is recorded: the first and NVMLA_TRACE_TILE (1 unless
+// the build sets it)
+#ifndef NVMLA_TRACE_TILE
+#define NVMLA_TRACE_TILE 1
+#endif
+#define NVMLA_TRACED_TILE(i) ((i) == 0 || (i) == NVMLA_TRACE_TILE)
+#define NVMLA_TRACE_SLOT(i) ((i) == 0 ? 0 : 1)
 #else
+#define NVMLA_TRACE_TILE (-1)
+#define NVMLA_TRACED_TILE(i) false
+#define NVMLA_TRACE_SLOT(i) 0
 #define NVMLA_TRACE_POINT(id) \
   do {                        \
   } while (0)
 #define NVMLA_TRACE_AFTER(id, v) \
+  do {                           \
+  } while (0)
+#define NVMLA_TRACE_VALUE(id, v) \
   do {                           \
   } while (0)
 #endif
@@ -106,23 +132,23 @@ __device__ unsigned long long nvmla_tc_trace[kTraceCtas][kTracePoints];
 constexpr int kTile = 128;              // rows per tile (MMA M)
 constexpr int kHeads = 64;              // heads per CTA (MMA N)
 constexpr int kMaxTiles = 16;           // 2048 slots
-constexpr int kWorkers = 512;           // warps 0-15
-constexpr int kMmaWarp = 16;            // allocates TMEM; lane 0 issues the MMAs
-constexpr int kThreads = 544;           // 17 warps
+constexpr int kThreads = 512;           // 16 warps, all workers
+constexpr int kMmaWarp = 15;            // allocates TMEM; its lane 0 also issues the MMAs
 constexpr int kMaxCluster = 16;         // CTAs sharing one token
 constexpr int kChunkBytes = 16384;      // 128 rows x 64 fp16 dims, 128B-swizzled
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;           // S^T: columns [0, 64)
 constexpr uint32_t kColO = 64;          // O^T block j: columns [64 + 64 j, +64)
 constexpr uint32_t kColR = 320;         // RoPE K: 32 columns (64 fp16 dims x 128 rows)
+constexpr int kPrefetchAhead = 3;       // tiles whose rows are prefetched into L2 ahead of use
 constexpr float kTau = 15.0f;           // rescale threshold, log2 units: P < 2^15 fits fp16
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr int kQBytes = kHeads * kDqk * 2;        // raw bf16 query block: 72 KB
 
 // shared memory map (bytes); the base is 1 KB aligned
 constexpr int kOffQ = 0;                              // Q^T: 9 chunks x 8 KB, K-major, swizzled
-constexpr int kOffKV = kOffQ + 9 * 8192;              // latent tile: 8 chunks x 16 KB; first the raw
-                                                      // query block, last the staged partial
+constexpr int kOffKV = kOffQ + 9 * 8192;              // latent tile: 8 chunks x 16 KB; first the
+                                                      // first tile's raw rows, last the staged partial
 constexpr int kOffP = kOffKV + 8 * kChunkBytes;       // P^T 16 KB, later the combine weights
 constexpr int kOffSlots = kOffP + kChunkBytes;        // kMaxTiles x 128 int32
 constexpr int kOffRed = kOffSlots + kMaxTiles * kTile * 4;  // 4 quadrants x 64 heads fp32
@@ -131,20 +157,19 @@ constexpr int kOffAlpha = kOffM + kHeads * 4;         // 64 fp32 rescale factors
 constexpr int kOffMl = kOffAlpha + kHeads * 4;        // 64 x (m, l) of this CTA
 constexpr int kOffBar = kOffMl + kHeads * 8;
 enum Bar {
-  kBarQ = 0,       // the raw query block has landed (TMA)
-  kBarKV = 1,      // the tile's latent chunks and RoPE K are written (16 worker warps)
-  kBarS = 2,       // QK done: S^T full; also every earlier MMA done (commit)
-  kBarP = 3,       // P^T written, O^T rescaled if needed (16 worker warps)
-  kBarPV = 4,      // 4: PV block j done, its two latent chunks reusable (commit)
-  kBarDrain = 8,   // every MMA finished (commit)
-  kBarRows0 = 9,   // NVFP4: the first tile's rows have landed (TMA; one arrival per row)
-  kNumBars = 10
+  kBarKV = 0,      // the tile's latent chunks and RoPE K are written (16 warps)
+  kBarS = 1,       // QK done: S^T full; also every earlier MMA done (commit)
+  kBarP = 2,       // P^T written, O^T rescaled if needed (16 warps)
+  kBarPV = 3,      // 4: PV block j done, its two latent chunks reusable (commit)
+  kBarDrain = 7,   // every MMA finished (commit)
+  kBarRows0 = 8,   // NVFP4: the first tile's rows have landed (TMA; one arrival per row)
+  kNumBars = 9
 };
 constexpr int kOffMisc = kOffBar + kNumBars * 8;      // tmem base, abort flag
 constexpr int kSmemBytes = kOffMisc + 16;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kOffKV % 1024 == 0 && kOffP % 1024 == 0, "swizzled operands need 1 KB alignment");
-static_assert(kQBytes == 9 * 8192, "the raw query block lands in the Q^T space and is converted in place");
+static_assert(kQBytes == 9 * 8192, "Q^T is nine 8 KB chunks");
 // NVFP4: the first tile's 128 rows land by TMA in the latent tile's space,
 // 368 bytes apart (23 units of 16 bytes: the rows of 32 consecutive lanes
 // fall into distinct banks)
@@ -169,7 +194,7 @@ struct Params {
   int num_splits;     // == cluster size
   int tiles_total;
   int32_t* err_word;
-  uint32_t p_wait_ns;  // limit of the MMA thread's wait for P^T; 0 = the default
+  uint32_t p_wait_ns;  // limit of the MMA issuer's wait for P^T; 0 = the default
   int force_p_timeout; // test hook: that wait gives up at once
 };
 
@@ -579,25 +604,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
 
   if (tid == 0) NVMLA_TRACE_POINT(0);
 
-  // ---- the query block (bf16, 64 KB latent + 8 KB RoPE, contiguous in
-  // global memory) is requested first, with two TMA bulk loads into the
-  // latent tile's space; the workers convert it once it has landed
-  if (tid == 0) {
-    mbar_init(bar(kBarQ), 1);
-    mbar_init(bar(kBarRows0), kTile);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    fence_async_smem();
-    mbar_arrive_expect_tx(bar(kBarQ), kQBytes);
-    const int64_t qh0 = static_cast<int64_t>(t) * p.H + h0;
-    bulk_load(sbase + kOffQ, p.q_latent + qh0 * kLatent, kHeads * kLatent * 2, bar(kBarQ));
-    bulk_load(sbase + kOffQ + kHeads * kLatent * 2, p.q_rope + qh0 * kRope, kHeads * kRope * 2, bar(kBarQ));
-  }
-  // the first tile's row barrier is initialised before any thread arrives on it
-  __syncthreads();
-
-  const bool is_worker = tid < kWorkers;
-  const int quad = warp & 3, qu = (warp >> 2) & 3;  // workers: TMEM lane quadrant, row quarter
-  const int r = quad * 32 + lane;                    // workers: row of the tile
+  const int quad = warp & 3, qu = warp >> 2;  // TMEM lane quadrant, row quarter
+  const int r = quad * 32 + lane;             // row of the tile
   const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
   const bool report = blockIdx.z == 0;               // one head block reports bad entries
 
@@ -607,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
   int32_t pos0 = -1;
   constexpr int kLaterPer = kMaxTiles / 4;  // later tiles per worker thread
   int32_t posl[kLaterPer];
-  if (is_worker) {
+  {
     if (kbeg + r < kend) pos0 = ldg_nc_s32(tk_row + kbeg + r);
 #pragma unroll
     for (int m = 0; m < kLaterPer; ++m) {
@@ -616,6 +624,28 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
       posl[m] = (i < ntiles && key < kend) ? ldg_nc_s32(tk_row + key) : -1;
     }
   }
+  // ---- the query block (bf16, 64 KB latent + 8 KB RoPE for the CTA's 64
+  // heads, each part contiguous in global memory), requested right after the
+  // slot-list entries, straight into registers: 16-byte unit u = tid + 512 m
+  // (m < 8) of the latent part, unit tid of the RoPE part. It is converted
+  // to fp16 Q^T while the first tile's rows are on their way; the TMA unit
+  // is left to those rows.
+  uint32_t qv[9][4];
+  {
+    const int64_t qh0 = static_cast<int64_t>(t) * p.H + h0;
+    const uint8_t* ql = reinterpret_cast<const uint8_t*>(p.q_latent + qh0 * kLatent);
+    const uint8_t* qr = reinterpret_cast<const uint8_t*>(p.q_rope + qh0 * kRope);
+#pragma unroll
+    for (int m = 0; m < 8; ++m) ldg_nc_v4(ql + 16 * (tid + kThreads * m), qv[m]);
+    ldg_nc_v4(qr + 16 * tid, qv[8]);
+  }
+  static_assert(kQBytes == 9 * kThreads * 16, "nine 16-byte units of the query block per thread");
+  if (tid == 0) {
+    mbar_init(bar(kBarRows0), kTile);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  // the first tile's row barrier is initialised before any thread arrives on it
+  __syncthreads();
   // ---- level 2: block-table entries (page index clamped into the row, so
   // the load is in bounds whatever the entry) and the sequence length
   const bool seq_ok = seq_raw >= 0 && seq_raw < p.sel.num_seqs;
@@ -652,7 +682,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
   int32_t page0 = 0;
   int32_t pagel[kLaterPer];
   if (tid == 0) NVMLA_TRACE_AFTER(25, pos0);
-  if (is_worker) {
+  {
     page0 = page_of(pos0);
     if (tid == 0) NVMLA_TRACE_AFTER(26, page0);
 #pragma unroll
@@ -669,9 +699,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
   // into shared memory, issued by the row's quarter-0 thread; FP8: this
   // thread's quarter of its row into registers); the later tiles' slots into
   // shared memory, their rows prefetched into L2
-  Quarter<FMT> raw;
+  Quarter<FMT> raw;   // the row quarter of the tile unpacked next
+  Quarter<FMT> rawn;  // NVFP4: the one after it, requested a tile ahead
   int32_t slot0 = -1;
-  if (is_worker) {
+  {
     const bool mine = ntiles > 0 && kbeg + r < kend;
     const int32_t sspec = mine ? phys_slot(pos0, page0) : -1;
     if constexpr (FMT == kFmtNvfp4) {
@@ -696,7 +727,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
       if (i < ntiles) {
         const int32_t sl = classify(posl[m], pagel[m], limit, report);
         slots[i * kTile + r] = sl;
-        if (sl >= 0) prefetch_l2(row_of(sl), kRB);
+        // the rows of the next three tiles into L2 now, the later ones three
+        // tiles ahead of their use (all at once, they would flood the memory
+        // system at start-up when a CTA has many tiles)
+        if (sl >= 0 && i <= kPrefetchAhead) prefetch_l2(row_of(sl), kRB);
       }
     }
   }
@@ -728,10 +762,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
   if (*abort_flag && tid == 0) report_error(p.err_word, NVMLA_ERRW_WAIT_TIMEOUT, 1);
   bool ok = *abort_flag == 0;
 
-  if (is_worker) {
+  {
     // ------------------------------------------------------------ workers
-    // query block -> fp16 Q^T, K-major 128B-swizzled (4608 pieces of 16
-    // bytes), out of the latent tile's space
+    // ---- the query block -> fp16 Q^T, K-major 128B-swizzled: latent unit
+    // u holds head u / 64, dims 8 (u % 64)..+7 (query chunk (u % 64) / 8);
+    // RoPE unit u holds head u / 8, RoPE dims 8 (u % 8)..+7 (query chunk 8)
+#pragma unroll
+    for (int m = 0; m < 9; ++m) {
+      const int u = tid + kThreads * m;
+      const int h = m < 8 ? u >> 6 : tid >> 3;
+      const int c = m < 8 ? (u & 63) >> 3 : 8;
+      const int q = m < 8 ? u & 7 : tid & 7;
+      uint32_t o[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        o[e] = pack_f16x2(bf16_bits_to_f32(qv[m][e] & 0xffffu), bf16_bits_to_f32(qv[m][e] >> 16));
+      *reinterpret_cast<uint4*>(smem + kOffQ + c * 8192 + swz(h, q)) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if (tid == 0) NVMLA_TRACE_POINT(3);
     if constexpr (FMT == kFmtNvfp4) {
       // this thread's quarter of its first-tile row, out of shared memory
       ok = ok && wait_bar_warp(bar(kBarRows0), 0, abort_flag, p.err_word);
@@ -758,7 +806,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
     if (tid == 0) NVMLA_TRACE_POINT(29);
     // every worker holds its first-tile row before the tile's space is written
     ok = !workers_sync_or(!ok);
-    if (tid == 0) NVMLA_TRACE_POINT(3);
+    if (tid == 0) NVMLA_TRACE_POINT(39);
 
     float lp[16];  // this row's share of its heads' sums
 #pragma unroll
@@ -775,45 +823,68 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
       store_rope<FMT>(raw, valid, rope_col);
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
     };
-    // ---- the first tile is unpacked while the query block is still landing
+    // ---- the first tile
     if (ok && ntiles > 0) unpack(slots[r] >= 0);
     if (tid == 0) NVMLA_TRACE_POINT(30);
-    // ---- the query block -> fp16 Q^T, K-major 128B-swizzled, in place: this
-    // thread's 9 pieces of 16 bytes into registers, a barrier, then converted
-    // to their swizzled places
-    {
-      bool okq = ok && wait_bar_warp(bar(kBarQ), 0, abort_flag, p.err_word);
-      if (tid == 0) NVMLA_TRACE_POINT(2);
-      uint4 qv[9];
-      if (okq) {
-#pragma unroll
-        for (int m = 0; m < 9; ++m) {
-          const int it = tid + kWorkers * m, h = it / 72, j = it - (it / 72) * 72;
-          qv[m] = *reinterpret_cast<const uint4*>(
-              smem + kOffQ +
-              (j < 64 ? h * (kLatent * 2) + 16 * j : kHeads * kLatent * 2 + h * (kRope * 2) + 16 * (j - 64)));
-        }
-      }
-      okq = !workers_sync_or(!okq);
-      if (okq) {
-#pragma unroll
-        for (int m = 0; m < 9; ++m) {
-          const int it = tid + kWorkers * m, h = it / 72, j = it - (it / 72) * 72, c = j >> 3, q = j & 7;
-          const uint32_t w[4] = {qv[m].x, qv[m].y, qv[m].z, qv[m].w};
-          uint32_t o[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) o[e] = pack_f16x2(bf16_bits_to_f32(w[e] & 0xffffu), bf16_bits_to_f32(w[e] >> 16));
-          *reinterpret_cast<uint4*>(smem + kOffQ + c * 8192 + swz(h, q)) = make_uint4(o[0], o[1], o[2], o[3]);
-        }
-      }
-      ok = okq;
-      if (tid == 0) NVMLA_TRACE_POINT(3);
-    }
     if (ok && ntiles > 0) {
       fence_async_smem();
       tc_fence_before();
       warp_arrive(bar(kBarKV), lane);
     }
+    // ---- MMA issue, by lane 0 of warp kMmaWarp between its own worker
+    // steps: a tile's QK right after the warp's arrival on kBarKV, its PV
+    // right after the warp's arrival on kBarP. The warp unpacks quarter 3,
+    // which waits for the last PV block of the previous tile in any case.
+    // Each run is unrolled straight-line code: a wait or a branch between two
+    // tcgen05.mma instructions stalls the issuer for about as long as an MMA.
+    const bool issuer = warp == kMmaWarp && lane == 0;
+    bool mok = true;  // issuer: no wait of its own has failed
+    auto issue_qk = [&](int i) {
+      mok = mok && wait_bar(bar(kBarKV), i & 1, abort_flag, p.err_word);
+      if (!mok) return;
+      tc_fence_after();
+      if (NVMLA_TRACED_TILE(i)) NVMLA_TRACE_POINT(7 + 8 * NVMLA_TRACE_SLOT(i));
+      // latent chunks c = 0..7 (A: the tile, K-major), then the RoPE K (A:
+      // TMEM); query chunk c is the B operand
+      constexpr uint32_t idesc_qk = idesc_f16(false, false);
+      const uint64_t a_kv = sdesc(sbase + kOffKV, 16, 1024);
+      const uint64_t b_q = sdesc(sbase + kOffQ, 16, 1024);
+      mma_chunk_qk<0 * 1024, 0 * 512>(tmem + kColS, a_kv, b_q, idesc_qk, 0);
+      mma_chunk_qk<1 * 1024, 1 * 512>(tmem + kColS, a_kv, b_q, idesc_qk, 1);
+      mma_chunk_qk<2 * 1024, 2 * 512>(tmem + kColS, a_kv, b_q, idesc_qk, 1);
+      mma_chunk_qk<3 * 1024, 3 * 512>(tmem + kColS, a_kv, b_q, idesc_qk, 1);
+      mma_chunk_qk<4 * 1024, 4 * 512>(tmem + kColS, a_kv, b_q, idesc_qk, 1);
+      mma_chunk_qk<5 * 1024, 5 * 512>(tmem + kColS, a_kv, b_q, idesc_qk, 1);
+      mma_chunk_qk<6 * 1024, 6 * 512>(tmem + kColS, a_kv, b_q, idesc_qk, 1);
+      mma_chunk_qk<7 * 1024, 7 * 512>(tmem + kColS, a_kv, b_q, idesc_qk, 1);
+      mma_chunk_qk_tmem<8 * 512>(tmem + kColS, tmem + kColR, b_q, idesc_qk);
+      mma_commit(bar(kBarS));
+      if (NVMLA_TRACED_TILE(i)) NVMLA_TRACE_POINT(9 + 8 * NVMLA_TRACE_SLOT(i));
+    };
+    auto issue_pv = [&](int i) {
+      const uint64_t p_limit = p.p_wait_ns ? p.p_wait_ns : kWaitLimitNs;
+      mok = mok && (p.force_p_timeout ? give_up(abort_flag, p.err_word)
+                                      : wait_bar(bar(kBarP), i & 1, abort_flag, p.err_word, p_limit));
+      if (!mok) return;
+      tc_fence_after();
+      if (NVMLA_TRACED_TILE(i)) NVMLA_TRACE_POINT(8 + 8 * NVMLA_TRACE_SLOT(i));
+      // block j: value dims 128j..128j+127 = latent chunks 2j, 2j+1 (A: V^T,
+      // MN-major, the two 64-dim halves one chunk apart; B: P^T), 8 steps of
+      // 16 rows, committed on its own
+      constexpr uint32_t idesc_pv = idesc_f16(true, true);
+      const uint64_t a_v = sdesc(sbase + kOffKV, kChunkBytes, 1024);
+      const uint64_t b_p = sdesc(sbase + kOffP, 8192, 1024);
+      const uint32_t acc = i != 0;
+      mma_block_pv<0 * 2048>(tmem + kColO + 0 * 64, a_v, b_p, idesc_pv, acc);
+      mma_commit(bar(kBarPV + 0));
+      mma_block_pv<1 * 2048>(tmem + kColO + 1 * 64, a_v, b_p, idesc_pv, acc);
+      mma_commit(bar(kBarPV + 1));
+      mma_block_pv<2 * 2048>(tmem + kColO + 2 * 64, a_v, b_p, idesc_pv, acc);
+      mma_commit(bar(kBarPV + 2));
+      mma_block_pv<3 * 2048>(tmem + kColO + 3 * 64, a_v, b_p, idesc_pv, acc);
+      mma_commit(bar(kBarPV + 3));
+      if (NVMLA_TRACED_TILE(i)) NVMLA_TRACE_POINT(10 + 8 * NVMLA_TRACE_SLOT(i));
+    };
     for (int i = 0; i < ntiles && ok; ++i) {
       const bool valid = slots[i * kTile + r] >= 0;
       // ---- unpack tile i: chunks 2qu, 2qu + 1 once PV block qu of the
@@ -822,23 +893,31 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
       bool okw = true;
       if (i >= 1) {
         okw = wait_bar_warp(bar(kBarPV + qu), (i - 1) & 1, abort_flag, p.err_word);
+        if (tid == 0 && i == NVMLA_TRACE_TILE) NVMLA_TRACE_POINT(36);
         if (okw) {
           unpack(valid);
+          if (tid == 0 && i == NVMLA_TRACE_TILE) NVMLA_TRACE_POINT(37);
           fence_async_smem();
           tc_fence_before();
           warp_arrive(bar(kBarKV), lane);
+          if constexpr (FMT == kFmtNvfp4) {
+            if (i + 1 < ntiles) raw = rawn;
+          }
         }
       }
-      if (tid == 0 && i < 2) NVMLA_TRACE_POINT(4 + 8 * i);
+      if (tid == 0 && NVMLA_TRACED_TILE(i)) NVMLA_TRACE_POINT(4 + 8 * NVMLA_TRACE_SLOT(i));
+      // ---- QK of tile i (the other lanes of the issuer's warp wait for it
+      // in the warp barrier of the next wait)
+      if (issuer && okw) issue_qk(i);
       // ---- softmax of tile i
       if (okw) okw = wait_bar_warp(bar(kBarS), i & 1, abort_flag, p.err_word);
-      if (tid == 0 && i < 2) NVMLA_TRACE_POINT(11 + 8 * i);
+      if (tid == 0 && NVMLA_TRACED_TILE(i)) NVMLA_TRACE_POINT(11 + 8 * NVMLA_TRACE_SLOT(i));
       if (workers_sync_or(!okw)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      if (tid == 0 && i < 2) NVMLA_TRACE_POINT(5 + 8 * i);
+      if (tid == 0 && NVMLA_TRACED_TILE(i)) NVMLA_TRACE_POINT(5 + 8 * NVMLA_TRACE_SLOT(i));
       float s[16];
       tmem_ld16f(tmem + lane_base + kColS + hb, s);
 #pragma unroll
@@ -934,12 +1013,38 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
       fence_async_smem();
       tc_fence_before();
       warp_arrive(bar(kBarP), lane);
-      // ---- the next tile's row into the same registers
-      if (i + 1 < ntiles) {
-        const int32_t ns = slots[(i + 1) * kTile + r];
-        if (ns >= 0) load_quarter<FMT>(raw, row_of(ns), qu);
+      // ---- a later tile's rows into L2, kPrefetchAhead tiles ahead
+      if (qu == 0 && i + 1 + kPrefetchAhead < ntiles) {
+        const int32_t ps = slots[(i + 1 + kPrefetchAhead) * kTile + r];
+        if (ps >= 0) prefetch_l2(row_of(ps), kRB);
       }
-      if (tid == 0 && i < 2) NVMLA_TRACE_POINT(6 + 8 * i);
+      // ---- rows of later tiles, requested after the softmax so that they do
+      // not land during this tile's QK (the MMAs read their operands from
+      // shared memory, and returning loads slow them). NVFP4 keeps two tiles
+      // in flight: after the first softmax the next two tiles' rows, then
+      // each time the one two tiles ahead (the next is already in raw); the
+      // wider FP8 rows keep one.
+      if constexpr (FMT == kFmtNvfp4) {
+        if (i == 0 && 1 < ntiles) {
+          const int32_t ns = slots[kTile + r];
+          if (ns >= 0) load_quarter<FMT>(raw, row_of(ns), qu);
+        }
+        if (i + 2 < ntiles) {
+          const int32_t ns = slots[(i + 2) * kTile + r];
+          if (ns >= 0) load_quarter<FMT>(rawn, row_of(ns), qu);
+        }
+      } else {
+        if (i + 1 < ntiles) {
+          const int32_t ns = slots[(i + 1) * kTile + r];
+          if (ns >= 0) load_quarter<FMT>(raw, row_of(ns), qu);
+        }
+      }
+      if (tid == 0 && NVMLA_TRACED_TILE(i)) NVMLA_TRACE_POINT(6 + 8 * NVMLA_TRACE_SLOT(i));
+      // ---- PV of tile i
+      if (warp == kMmaWarp) {
+        if (issuer) issue_pv(i);
+        __syncwarp();
+      }
     }
     // ------------------------------------------------------------ row sums
     ok = !workers_sync_or(!ok);
@@ -1009,65 +1114,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
     }
     tc_fence_before();
     if (tid == 0) NVMLA_TRACE_POINT(21);
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issue
-    // One thread issues every MMA in unrolled straight-line sequences: a
-    // wait or a branch between two tcgen05.mma instructions stalls the
-    // issuer for about as long as an MMA, so it waits once before a tile's
-    // QK and once before its PV.
-    if (lane == 0) {
-      constexpr uint32_t idesc_qk = idesc_f16(false, false);
-      constexpr uint32_t idesc_pv = idesc_f16(true, true);
-      // base descriptors: the latent tile K-major (QK's A), the same tile
-      // MN-major with its 64-dim halves one chunk apart (PV's A), Q^T, P^T
-      const uint64_t a_kv = sdesc(sbase + kOffKV, 16, 1024);
-      const uint64_t a_v = sdesc(sbase + kOffKV, kChunkBytes, 1024);
-      const uint64_t b_q = sdesc(sbase + kOffQ, 16, 1024);
-      const uint64_t b_p = sdesc(sbase + kOffP, 8192, 1024);
-      bool mok = ok;
-      const uint64_t p_limit = p.p_wait_ns ? p.p_wait_ns : kWaitLimitNs;
-      for (int i = 0; i < ntiles && mok; ++i) {
-        mok = wait_bar(bar(kBarKV), i & 1, abort_flag, p.err_word);
-        if (!mok) break;
-        tc_fence_after();
-        if (i < 2) NVMLA_TRACE_POINT(7 + 8 * i);
-        // QK: latent chunks c = 0..7 (A from the tile), then the RoPE K (A
-        // from TMEM); query chunk c is the B operand
-        mma_chunk_qk<0 * 1024, 0 * 512>(tmem + kColS, a_kv, b_q, idesc_qk, 0);
-        mma_chunk_qk<1 * 1024, 1 * 512>(tmem + kColS, a_kv, b_q, idesc_qk, 1);
-        mma_chunk_qk<2 * 1024, 2 * 512>(tmem + kColS, a_kv, b_q, idesc_qk, 1);
-        mma_chunk_qk<3 * 1024, 3 * 512>(tmem + kColS, a_kv, b_q, idesc_qk, 1);
-        mma_chunk_qk<4 * 1024, 4 * 512>(tmem + kColS, a_kv, b_q, idesc_qk, 1);
-        mma_chunk_qk<5 * 1024, 5 * 512>(tmem + kColS, a_kv, b_q, idesc_qk, 1);
-        mma_chunk_qk<6 * 1024, 6 * 512>(tmem + kColS, a_kv, b_q, idesc_qk, 1);
-        mma_chunk_qk<7 * 1024, 7 * 512>(tmem + kColS, a_kv, b_q, idesc_qk, 1);
-        mma_chunk_qk_tmem<8 * 512>(tmem + kColS, tmem + kColR, b_q, idesc_qk);
-        mma_commit(bar(kBarS));
-        if (i < 2) NVMLA_TRACE_POINT(9 + 8 * i);
-        mok = p.force_p_timeout ? give_up(abort_flag, p.err_word)
-                                : wait_bar(bar(kBarP), i & 1, abort_flag, p.err_word, p_limit);
-        if (!mok) break;
-        tc_fence_after();
-        if (i < 2) NVMLA_TRACE_POINT(8 + 8 * i);
-        // PV block j: value dims 128j..128j+127 = latent chunks 2j, 2j+1
-        // (MN-major V^T, the two 64-dim halves one chunk apart), 8 steps of
-        // 16 rows; each block is committed on its own
-        const uint32_t acc = i != 0;
-        mma_block_pv<0 * 2048>(tmem + kColO + 0 * 64, a_v, b_p, idesc_pv, acc);
-        mma_commit(bar(kBarPV + 0));
-        mma_block_pv<1 * 2048>(tmem + kColO + 1 * 64, a_v, b_p, idesc_pv, acc);
-        mma_commit(bar(kBarPV + 1));
-        mma_block_pv<2 * 2048>(tmem + kColO + 2 * 64, a_v, b_p, idesc_pv, acc);
-        mma_commit(bar(kBarPV + 2));
-        mma_block_pv<3 * 2048>(tmem + kColO + 3 * 64, a_v, b_p, idesc_pv, acc);
-        mma_commit(bar(kBarPV + 3));
-        if (i < 2) NVMLA_TRACE_POINT(10 + 8 * i);
+    // every MMA the issuer issued has finished once this commit lands (the
+    // epilogue has waited for the last PV; after an abort, anything issued)
+    if (warp == kMmaWarp) {
+      if (issuer) {
+        mma_commit(bar(kBarDrain));
+        wait_bar_drain(bar(kBarDrain), 0);
       }
-      // every MMA this thread issued has finished once this commit lands
-      mma_commit(bar(kBarDrain));
-      wait_bar_drain(bar(kBarDrain), 0);
+      __syncwarp();
     }
-    __syncwarp();
   }
 
   // ------------------------------------------------------------ combine
@@ -1076,12 +1131,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
   }
-  // the query block's and the first tile's copies have landed before this
-  // CTA's shared memory can go
-  if (tid == 0) {
-    wait_bar_drain(bar(kBarQ), 0);
-    if (FMT == kFmtNvfp4) wait_bar_drain(bar(kBarRows0), 0);
-  }
+  // the first tile's copies have landed before this CTA's shared memory can go
+  if (tid == 0 && FMT == kFmtNvfp4) wait_bar_drain(bar(kBarRows0), 0);
   if (S > 1) {
     // release / acquire at cluster scope: every CTA's staged partial and
     // (m, l) are visible to every CTA of the cluster
@@ -1159,7 +1210,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
 #pragma unroll
       for (int e = 0; e < 8; ++e) tb[(8 * v + e) * pitch + 8 * ((dd >> 3) ^ v) + (dd & 7)] = __float2bfloat16_rn(acc[e]);
     }
+    if (tid == 0) NVMLA_TRACE_POINT(33);
     __syncthreads();
+    if (tid == 0) NVMLA_TRACE_POINT(34);
     // out rows of this CTA's dims, 16 bytes a thread: a warp writes whole
     // 128-byte runs of a head row
     const int upr = D / 8;  // 16-byte units per head row
@@ -1168,6 +1221,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
       *reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(t) * p.H + h0 + h) * kLatent + d0 + 8 * c) =
           *reinterpret_cast<const uint4*>(tb + h * pitch + 8 * (c ^ (h >> 3)));
     }
+    if (tid == 0) NVMLA_TRACE_POINT(35);
     // no CTA leaves while another may still read its shared memory
     cluster_sync_all();
   }
