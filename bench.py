@@ -837,8 +837,10 @@ def main():
             tev.append(e)
         torch.cuda.synchronize()
         t_us = statistics.mean([e[0].elapsed_time(e[1]) for e in tev]) * 1e3
+        t_kernel = kernel_only_us(lambda: nvmla.nvmla_topk_select(sc, w.topk, out=tko), flush)
         topk_sel = {"us_per_call": t_us, "T": w.T, "candidates": ctx, "topk": w.topk,
-                    "score_bytes": w.T * ctx * 4, "gbs": w.T * ctx * 4 / (t_us * 1e-6) / 1e9}
+                    "score_bytes": w.T * ctx * 4, "gbs": w.T * ctx * 4 / (t_us * 1e-6) / 1e9,
+                    "kernel_only": t_kernel}
         del sc
 
     # ---------------- pack of the write+read workload's 6144-token chunk
@@ -861,6 +863,7 @@ def main():
     torch.cuda.synchronize()
     pack_us = statistics.mean([pk[2 * i].elapsed_time(pk[2 * i + 1]) for i in range(K)]) * 1e3
     pack_bytes = 6144 * (1152 + 352 + 4)
+    pack_kernel = kernel_only_us(lambda: nvmla.nvfp4_mla_pack(plat, prope, pslots, pcache), flush)
 
     # ---------------- the other workloads the baseline names, same protocol
     configs = None
@@ -911,8 +914,11 @@ def main():
         "decode_kernel_only": dec_kernel,
         "decode_us": {"mean": dec_us, "median": statistics.median(dec_ms) * 1e3, "min": min(dec_ms) * 1e3},
         "pack_step_us": statistics.mean(pack_ms) * 1e3,
-        "pack_chunk": {"tokens": 6144, "us_per_call": pack_us, "gbs": pack_bytes / (pack_us * 1e-6) / 1e9,
-                       "frac_hbm": pack_bytes / (pack_us * 1e-6) / 1e9 / bw},
+        "pack_chunk": {"tokens": 6144, "bytes": pack_bytes, "us_per_call": pack_us,
+                       "gbs": pack_bytes / (pack_us * 1e-6) / 1e9,
+                       "frac_hbm": pack_bytes / (pack_us * 1e-6) / 1e9 / bw,
+                       "kernel_only": pack_kernel,
+                       "frac_hbm_kernel": pack_bytes / (pack_kernel["cold_l2_us"] * 1e-6) / 1e9 / bw},
         "staged": staged,
         "layered": layered,
         "topk_select": (dict(topk_sel, frac_hbm=topk_sel["gbs"] / bw) if topk_sel else None),

@@ -69,14 +69,25 @@ nvmla_status counted(cudaError_t e, int kernels, const char* what) {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// SM count of the current device, queried once per device (concurrent
+// callers may each query it; all store the same value); without a device,
+// the 152 of a GB300, so that host-only callers (split counts, workspace
+// sizes) see the shapes the device would use
 int num_sms() {
+  static std::atomic<int> cached[kMaxHostDevices];
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 152;
-  static int cached[64] = {0};
-  if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
-  int n = 152;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) n = 152;
-  if (dev >= 0 && dev < 64) cached[dev] = n;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxHostDevices) {
+    cudaGetLastError();
+    return 152;
+  }
+  const int known = cached[dev].load(std::memory_order_relaxed);
+  if (known > 0) return known;
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    return 152;
+  }
+  cached[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 

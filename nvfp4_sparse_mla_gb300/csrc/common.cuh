@@ -6,6 +6,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "nvmla.h"
 
 namespace nvmla {
@@ -149,5 +151,41 @@ struct RowSelect {
     return s;
   }
 };
+
+// ---------------------------------------------------------------- launch shape
+
+constexpr int kMaxHostDevices = 64;
+
+// Blocks of `kernel` (with `threads` threads and `smem` bytes of dynamic
+// shared memory a block) that the current device holds at once: its SM
+// count times the blocks resident per SM. Queried once per device and kept
+// in `cache` (one slot per device, shared by concurrent callers: each
+// computes the same value); 0 if the device or the query fails.
+template <typename Kernel>
+inline int resident_blocks(Kernel kernel, int threads, size_t smem, std::atomic<int> (&cache)[kMaxHostDevices]) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxHostDevices) return 0;
+  const int known = cache[dev].load(std::memory_order_relaxed);
+  if (known > 0) return known;
+  int sms = 0, per_sm = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess || sms <= 0 ||
+      per_sm <= 0) {
+    cudaGetLastError();  // no sticky error from a failed query
+    return 0;
+  }
+  cache[dev].store(sms * per_sm, std::memory_order_relaxed);
+  return sms * per_sm;
+}
+
+// Grid of a grid-stride kernel: the blocks the work needs, at most one full
+// wave of resident blocks (all of them when the query fails).
+template <typename Kernel>
+inline int grid_blocks(int64_t needed, Kernel kernel, int threads, size_t smem, std::atomic<int> (&cache)[kMaxHostDevices]) {
+  const int64_t wave = resident_blocks(kernel, threads, smem, cache);
+  int64_t b = needed < 1 ? 1 : needed;
+  if (wave > 0 && b > wave) b = wave;
+  return static_cast<int>(b < 0x7fffffff ? b : 0x7fffffff);
+}
 
 }  // namespace nvmla

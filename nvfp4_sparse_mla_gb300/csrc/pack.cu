@@ -5,11 +5,14 @@
 // stored as 4-bit values with one FP8 scale per 16 values, the 64-value RoPE
 // part stays FP8, 352 bytes per row.
 //
-// One warp per token. Lane l owns latent group l (16 values = 32 bytes of
-// bf16, read as two 16-byte loads, so a warp reads the token's 1 KiB latent
-// fully coalesced) and RoPE values 2l, 2l+1. The group's scale and codes are
-// computed in registers without any shuffle; the 352-byte row is assembled
-// in shared memory and written as 22 aligned 16-byte stores.
+// One warp per token at a time, each warp taking every nwarps-th token and
+// fetching its next token's values while it quantises the current one (the
+// grid gives every warp at least two tokens, at most one wave). Lane l owns
+// latent group l (16 values = 32 bytes of bf16, read as two 16-byte loads,
+// so a warp reads the token's 1 KiB latent fully coalesced) and RoPE values
+// 2l, 2l+1. The group's scale and codes are computed in registers without
+// any shuffle; the 352-byte row is assembled in shared memory and written as
+// 22 aligned 16-byte stores.
 //
 // Rounding, bit-exact with the definition:
 //  * scale = E4M3(amax / 6): fp32 division correctly rounded (__fdiv_rn), then
@@ -18,11 +21,31 @@
 //    infinite binary expansion, so the fp32 rounding can never create or
 //    break an E4M3 tie: the two roundings equal one.
 //  * codes: |v| is compared with S times the E2M1 midpoints 0.25, 0.75, 1.25,
-//    1.75, 2.5, 3.5, 5 (products exact in fp32); at a midpoint the strict or
-//    non-strict comparison sends the value to the even code.
+//    1.75, 2.5, 3.5, 5; at a midpoint the strict or non-strict comparison
+//    sends the value to the even code. The comparisons run two values at a
+//    time in bf16x2 on the input itself: each product has at most 7
+//    significant bits and so is exact in bf16.
 #include "common.cuh"
 
 namespace nvmla {
+// read-only loads issued where they stand (volatile: the compiler does not
+// sink them to their first use)
+__device__ __forceinline__ uint4 ldg_nc_u4(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint32_t ldg_nc_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ int32_t ldg_nc_s32i(const int32_t* p) {
+  int32_t v;
+  asm volatile("ld.global.nc.s32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
 
 constexpr int kPackWarps = 8;
 
@@ -37,14 +60,33 @@ nvfp4_pack_kernel(const __nv_bfloat16* __restrict__ latent, int64_t lat_stride,
   uint8_t* row = rowbuf[wib];
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kPackWarps;
 
-  for (int64_t n = static_cast<int64_t>(blockIdx.x) * kPackWarps + wib; n < n_tokens; n += nwarps) {
-    // the token's values are requested together with its slot (one memory
-    // round trip, not two); a token that is skipped leaves them unused
+  // a token's values are requested together with its slot (one memory
+  // round trip, not two), and the warp's next token's before this one is
+  // quantised; a token that is skipped leaves them unused
+  struct In {
+    uint4 a, b;
+    uint32_t rw;
+    int32_t slot;
+  };
+  auto fetch = [&](int64_t n) {
+    In v;
     const uint4* src = reinterpret_cast<const uint4*>(latent + n * lat_stride + lane * 16);
-    const uint4 a = __ldg(src);
-    const uint4 b = __ldg(src + 1);
-    const uint32_t rw = __ldg(reinterpret_cast<const uint32_t*>(rope + n * rope_stride) + lane);
-    const int64_t slot = __ldg(slot_mapping + n);
+    v.a = ldg_nc_u4(src);
+    v.b = ldg_nc_u4(src + 1);
+    v.rw = ldg_nc_u32(reinterpret_cast<const uint32_t*>(rope + n * rope_stride) + lane);
+    v.slot = ldg_nc_s32i(slot_mapping + n);
+    return v;
+  };
+  int64_t n = static_cast<int64_t>(blockIdx.x) * kPackWarps + wib;
+  In cur;
+  if (n < n_tokens) cur = fetch(n);
+  for (; n < n_tokens; n += nwarps) {
+    In nxt{};
+    if (n + nwarps < n_tokens) nxt = fetch(n + nwarps);
+    const uint4 a = cur.a, b = cur.b;
+    const uint32_t rw = cur.rw;
+    const int64_t slot = cur.slot;
+    cur = nxt;
     if (slot < 0) continue;
     if (slot >= num_slots) {
       if (lane == 0) report_error(err_word, NVMLA_ERRW_PACK_SLOT, 1);
@@ -52,26 +94,49 @@ nvfp4_pack_kernel(const __nv_bfloat16* __restrict__ latent, int64_t lat_stride,
     }
     // ---- latent group `lane`
     const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-    float amax = 0.f;
+    // amax in bf16x2 (max ignores a NaN operand, as fmaxf does; an all-NaN
+    // group gets 0)
+    uint32_t mx = w[0] & 0x7fff7fffu;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w[i] & 0xffffu)));
-      amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w[i] >> 16)));
-    }
+    for (int i = 1; i < 8; ++i) asm("max.bf16x2 %0, %1, %2;" : "=r"(mx) : "r"(mx), "r"(w[i] & 0x7fff7fffu));
+    const float amax = fmaxf(0.f, fmaxf(bf16_bits_to_f32(mx & 0xffffu), bf16_bits_to_f32(mx >> 16)));
     const float q = __fdiv_rn(amax, 6.0f);
     const uint32_t sbyte = f32x2_to_e4m3x2(q, 0.f) & 0xffu;
     const float S = __half2float(__ushort_as_half(static_cast<uint16_t>(e4m3x2_to_f16x2(static_cast<uint16_t>(sbyte)) & 0xffffu)));
-    const float t0 = 0.25f * S, t1 = 0.75f * S, t2 = 1.25f * S, t3 = 1.75f * S;
-    const float t4 = 2.5f * S, t5 = 3.5f * S, t6 = 5.0f * S;
+    // codes two at a time in bf16x2, straight on the input: every threshold
+    // mid * S (mid = 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5: at most 3
+    // significant bits; S: 4) is exact in bf16. The count of thresholds
+    // below |v| is the code magnitude; at a midpoint the strict or non-strict
+    // comparison sends the value to the even code; a NaN compares false.
+    uint32_t th[7];
+    {
+      const float mids[7] = {0.25f, 0.75f, 1.25f, 1.75f, 2.5f, 3.5f, 5.0f};
+#pragma unroll
+      for (int k = 0; k < 7; ++k) {
+        const uint32_t tb = __float_as_uint(mids[k] * S) >> 16;
+        th[k] = tb | (tb << 16);
+      }
+    }
     uint32_t codes[2] = {0u, 0u};
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const uint32_t bits = (i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xffffu);
-      const float x = fabsf(bf16_bits_to_f32(bits));
-      uint32_t m = (x > t0) + (x >= t1) + (x > t2) + (x >= t3) + (x > t4) + (x >= t5) + (x > t6);
-      m = (S == 0.f) ? 0u : m;
-      const uint32_t c = m | ((bits >> 12) & 8u);
-      codes[i >> 3] |= c << (4 * (i & 7));
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t wi = w[i];
+      const uint32_t x2 = wi & 0x7fff7fffu;
+      uint32_t m2 = 0u;  // bf16x2 counts
+#pragma unroll
+      for (int k = 0; k < 7; ++k) {
+        uint32_t c;
+        if (k % 2 == 0)
+          asm("set.gt.bf16x2.bf16x2 %0, %1, %2;" : "=r"(c) : "r"(x2), "r"(th[k]));
+        else
+          asm("set.ge.bf16x2.bf16x2 %0, %1, %2;" : "=r"(c) : "r"(x2), "r"(th[k]));
+        asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(m2) : "r"(m2), "r"(c));
+      }
+      // count + 128 puts the count in the low mantissa bits of each half
+      asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(m2) : "r"(m2), "r"(0x43004300u));
+      m2 = (S == 0.f) ? 0u : (m2 & 0x000f000fu);
+      const uint32_t byte = (m2 & 0xfu) | ((m2 >> 12) & 0xf0u) | ((wi >> 12) & 0x8u) | ((wi >> 24) & 0x80u);
+      codes[i >> 2] |= byte << (8 * (i & 3));
     }
     *reinterpret_cast<uint2*>(row + 8 * lane) = make_uint2(codes[0], codes[1]);
     row[kScaleOff + lane] = static_cast<uint8_t>(sbyte);
@@ -89,8 +154,10 @@ nvfp4_pack_kernel(const __nv_bfloat16* __restrict__ latent, int64_t lat_stride,
 cudaError_t launch_pack(const void* latent, int64_t lat_stride, const void* rope, int64_t rope_stride,
                         const int32_t* slot_mapping, int64_t n_tokens, uint8_t* cache, int64_t num_pages,
                         int32_t page_rows, int32_t* err_word, cudaStream_t stream) {
-  const int64_t blocks_needed = (n_tokens + kPackWarps - 1) / kPackWarps;
-  const int blocks = static_cast<int>(blocks_needed < 152 * 16 ? blocks_needed : 152 * 16);
+  static std::atomic<int> wave[kMaxHostDevices];
+  // at least two tokens a warp (the second is fetched during the first)
+  const int blocks = grid_blocks((n_tokens + 2 * kPackWarps - 1) / (2 * kPackWarps), nvfp4_pack_kernel,
+                                 kPackWarps * 32, 0, wave);
   nvfp4_pack_kernel<<<blocks, kPackWarps * 32, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(latent), lat_stride, static_cast<const __nv_bfloat16*>(rope),
       rope_stride, slot_mapping, n_tokens, cache, num_pages * kPage, page_rows, err_word);
@@ -148,8 +215,8 @@ fp8_pack_kernel(const __nv_bfloat16* __restrict__ latent, int64_t lat_stride, co
 cudaError_t launch_fp8_pack(const void* latent, int64_t lat_stride, const void* rope, int64_t rope_stride,
                             const int32_t* slot_mapping, int64_t n_tokens, uint8_t* cache, int64_t num_pages,
                             int32_t* err_word, cudaStream_t stream) {
-  const int64_t blocks_needed = (n_tokens + kPackWarps - 1) / kPackWarps;
-  const int blocks = static_cast<int>(blocks_needed < 152 * 16 ? blocks_needed : 152 * 16);
+  static std::atomic<int> wave[kMaxHostDevices];
+  const int blocks = grid_blocks((n_tokens + kPackWarps - 1) / kPackWarps, fp8_pack_kernel, kPackWarps * 32, 0, wave);
   fp8_pack_kernel<<<blocks, kPackWarps * 32, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(latent), lat_stride, static_cast<const __nv_bfloat16*>(rope), rope_stride,
       slot_mapping, n_tokens, cache, num_pages * kPage, err_word);

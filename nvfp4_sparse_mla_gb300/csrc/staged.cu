@@ -59,8 +59,8 @@ stage_dequant_kernel(const uint8_t* __restrict__ cache, RowSelect sel, int T, ui
 cudaError_t launch_stage_dequant(const uint8_t* cache, const RowSelect& sel, int T, uint8_t* fp8_rows,
                                  int32_t* row_idx, int32_t* err_word, cudaStream_t stream) {
   const int64_t total = static_cast<int64_t>(T) * sel.topk;
-  const int64_t need = (total + kStageWarps - 1) / kStageWarps;
-  const int blocks = static_cast<int>(need < 152 * 16 ? need : 152 * 16);
+  static std::atomic<int> wave[kMaxHostDevices];
+  const int blocks = grid_blocks((total + kStageWarps - 1) / kStageWarps, stage_dequant_kernel, kStageWarps * 32, 0, wave);
   stage_dequant_kernel<<<blocks, kStageWarps * 32, 0, stream>>>(cache, sel, T, fp8_rows, row_idx, err_word);
   return cudaGetLastError();
 }

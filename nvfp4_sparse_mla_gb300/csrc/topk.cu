@@ -658,14 +658,16 @@ __global__ void __cluster_dims__(kTopkCtas, 1, 1) __launch_bounds__(kTopkThreads
 cudaError_t launch_topk_select(const float* scores, int64_t stride, int32_t ncols, const int32_t* lengths, int32_t T,
                                int32_t topk, int32_t* out, cudaStream_t stream) {
   constexpr int kDyn = static_cast<int>(sizeof(TopkShared));
-  static bool attr_set[64] = {false};  // the attribute is set once per device
+  // the attribute is set once per device; a caller that sees the flag (acquire)
+  // also sees the attribute set by the caller that raised it (release)
+  static std::atomic<bool> attr_set[kMaxHostDevices];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+  if (dev < 0 || dev >= kMaxHostDevices || !attr_set[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDyn);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    if (dev >= 0 && dev < kMaxHostDevices) attr_set[dev].store(true, std::memory_order_release);
   }
   topk_select_kernel<<<dim3(kTopkCtas, T), kTopkThreads, kDyn, stream>>>(scores, stride, ncols, lengths, topk, out);
   return cudaGetLastError();

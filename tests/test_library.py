@@ -197,3 +197,40 @@ def test_fp8_cache_calls_reject_bad_arguments(lib):
     args[12] = 64
     args[2] = P(0x10008)
     assert L.sparse_mla_decode_fp8cache(*args) == 1            # misaligned cache
+
+
+_CONCURRENT_QUERIES = r"""
+import ctypes, sys, threading
+import nvfp4_sparse_mla_gb300 as nvmla
+lib = nvmla.load()
+shapes = [(T, H, k) for T in (1, 7, 15, 24, 35, 64, 128, 320) for H in (16, 48, 64, 128) for k in (512, 2048)]
+def run():
+    return [(nvmla.sparse_mla_decode_workspace_size(T, H, k), nvmla.sparse_mla_decode_splits(T, H, k))
+            for (T, H, k) in shapes]
+start = threading.Barrier(8)
+results = [None] * 8
+def worker(i):
+    start.wait()
+    results[i] = [run() for _ in range(20)]
+threads = [threading.Thread(target=worker, args=(i,)) for i in range(8)]
+for t in threads: t.start()
+for t in threads: t.join()
+ref = run()
+bad = sum(r != ref for per in results for r in per)
+print("shapes", len(shapes), "mismatches", bad)
+sys.exit(1 if bad else 0)
+"""
+
+
+def test_size_queries_from_eight_threads_at_first_use(lib):
+    """A fresh process whose first calls into the library come from eight
+    threads at once (ctypes drops the GIL): each thread's workspace sizes and
+    split counts equal the ones a single thread sees afterwards. On a GPU this
+    races the per-device launch set-up; without one, the host-only model."""
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", _CONCURRENT_QUERIES], cwd=root, capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "mismatches 0" in r.stdout
