@@ -1077,38 +1077,57 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
     }
     workers_sync();
     if (tid == 0) NVMLA_TRACE_POINT(20);
-    // ------------------------------------------------------------ O^T, block by block as the last PV finishes
+    // ------------------------------------------------------------ O^T
+    // The last PV's block 3 commit lands after blocks 0-2 (a commit covers
+    // every MMA issued before it): one wait, then the four blocks' TMEM
+    // loads two at a time.
     bool have = ok && ntiles > 0;
-    for (int j = 0; j < 4; ++j) {
-      if (have) have = wait_bar_warp(bar(kBarPV + j), (ntiles - 1) & 1, abort_flag, p.err_word);
-      tc_fence_after();
-      float o[16];
+    if (have) have = wait_bar_warp(bar(kBarPV + 3), (ntiles - 1) & 1, abort_flag, p.err_word);
+    tc_fence_after();
+    float inv_l[16];  // 1 / l of this thread's heads (0 for an empty head)
+#pragma unroll
+    for (int h4 = 0; h4 < 4; ++h4) {
+      const float4 a4 = *reinterpret_cast<const float4*>(alpha_s + hb + 4 * h4);
+      inv_l[4 * h4] = a4.x;
+      inv_l[4 * h4 + 1] = a4.y;
+      inv_l[4 * h4 + 2] = a4.z;
+      inv_l[4 * h4 + 3] = a4.w;
+    }
+#pragma unroll
+    for (int j2 = 0; j2 < 4; j2 += 2) {
+      float o2[2][16];
       if (have) {
-        tmem_ld16f(tmem + lane_base + kColO + 64 * j + hb, o);
+        NVMLA_TMEM_LD16F(tmem + lane_base + kColO + 64 * j2 + hb, o2[0], 0);
+        NVMLA_TMEM_LD16F(tmem + lane_base + kColO + 64 * (j2 + 1) + hb, o2[1], 0);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
       } else {
 #pragma unroll
-        for (int e = 0; e < 16; ++e) o[e] = 0.f;
+        for (int e = 0; e < 16; ++e) o2[0][e] = o2[1][e] = 0.f;
       }
-      const int d = 128 * j + r;  // TMEM lane r of block j: value dim 128 j + r
-      if (S == 1) {
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
-          p.out[(static_cast<int64_t>(t) * p.H + h0 + hb + e) * kLatent + d] =
-              __float2bfloat16_rn(o[e] * alpha_s[hb + e]);
-      } else {
-        // normalised partial (fp16, [dim d][64 heads], 16-byte unit v of
-        // dim row d at v ^ (d & 7)) in the latent tile, which PV blocks
-        // 0..j no longer read
-        uint8_t* stg = smem + kOffKV + d * 128;
+      for (int jj = 0; jj < 2; ++jj) {
+        const int j = j2 + jj;
+        const float* o = o2[jj];
+        const int d = 128 * j + r;  // TMEM lane r of block j: value dim 128 j + r
+        if (S == 1) {
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          uint32_t w4[4];
+          for (int e = 0; e < 16; ++e)
+            p.out[(static_cast<int64_t>(t) * p.H + h0 + hb + e) * kLatent + d] = __float2bfloat16_rn(o[e] * inv_l[e]);
+        } else {
+          // normalised partial (fp16, [dim d][64 heads], 16-byte unit v of
+          // dim row d at v ^ (d & 7)) in the latent tile, which the PV no
+          // longer reads
+          uint8_t* stg = smem + kOffKV + d * 128;
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int hl = 8 * cc + 2 * e;
-            w4[e] = pack_f16x2(o[hl] * alpha_s[hb + hl], o[hl + 1] * alpha_s[hb + hl + 1]);
+          for (int cc = 0; cc < 2; ++cc) {
+            uint32_t w4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int hl = 8 * cc + 2 * e;
+              w4[e] = pack_f16x2(o[hl] * inv_l[hl], o[hl + 1] * inv_l[hl + 1]);
+            }
+            *reinterpret_cast<uint4*>(stg + (((2 * qu + cc) ^ (d & 7)) << 4)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
           }
-          *reinterpret_cast<uint4*>(stg + (((2 * qu + cc) ^ (d & 7)) << 4)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
         }
       }
     }
