@@ -162,7 +162,7 @@ enum Bar {
   kBarP = 2,       // P^T written, O^T rescaled if needed (16 warps)
   kBarPV = 3,      // 4: PV block j done, its two latent chunks reusable (commit)
   kBarDrain = 7,   // every MMA finished (commit)
-  kBarRows0 = 8,   // NVFP4: the first tile's rows have landed (TMA; one arrival per row)
+  kBarRows0 = 8,   // the first tile's rows have landed (TMA; one arrival per row)
   kNumBars = 9
 };
 constexpr int kOffMisc = kOffBar + kNumBars * 8;      // tmem base, abort flag
@@ -170,12 +170,13 @@ constexpr int kSmemBytes = kOffMisc + 16;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kOffKV % 1024 == 0 && kOffP % 1024 == 0, "swizzled operands need 1 KB alignment");
 static_assert(kQBytes == 9 * 8192, "Q^T is nine 8 KB chunks");
-// NVFP4: the first tile's 128 rows land by TMA in the latent tile's space,
-// 368 bytes apart (23 units of 16 bytes: the rows of 32 consecutive lanes
-// fall into distinct banks)
-constexpr int kRawPitch = 368;
+// The first tile's 128 rows land by TMA in the latent tile's space, an odd
+// number of 16-byte units apart (NVFP4 23, FP8 37), so that the rows of
+// eight consecutive lanes fall into distinct banks
+constexpr int kRawPitchNvfp4 = 368;  // 352-byte rows
+constexpr int kRawPitchFp8 = 592;    // 576-byte rows (37 units of 16 bytes)
 constexpr int kOffRaw0 = kOffKV;
-static_assert(kOffRaw0 + kTile * kRawPitch <= kOffKV + 8 * kChunkBytes, "first-tile rows fit the latent tile");
+static_assert(kOffRaw0 + kTile * kRawPitchFp8 <= kOffKV + 8 * kChunkBytes, "first-tile rows fit the latent tile");
 static_assert(kOffMl % 16 == 0, "(m, l) block alignment");
 
 // value dims [dim_lo(r), dim_lo(r + 1)) are combined by CTA r of S: whole
@@ -579,6 +580,7 @@ __device__ __forceinline__ void store_rope(const Quarter<FMT>& q, bool valid, ui
 template <int FMT>
 __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) {
   constexpr int kRB = FMT == kFmtFp8 ? kFp8RowBytes : kRowBytes;  // bytes per cache row
+  constexpr int kRawPitch = FMT == kFmtFp8 ? kRawPitchFp8 : kRawPitchNvfp4;  // first-tile rows in shared memory
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -695,28 +697,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
   }
   if (tid == 0) NVMLA_TRACE_AFTER(27, static_cast<int32_t>(limit));
 
-  // ---- level 3: the first tile's rows (NVFP4: one TMA bulk copy per row
-  // into shared memory, issued by the row's quarter-0 thread; FP8: this
-  // thread's quarter of its row into registers); the later tiles' slots into
-  // shared memory, their rows prefetched into L2
+  // ---- level 3: the first tile's rows, one TMA bulk copy per row into
+  // shared memory, issued by the row's quarter-0 thread; the later tiles'
+  // slots into shared memory, their rows prefetched into L2
   Quarter<FMT> raw;   // the row quarter of the tile unpacked next
   Quarter<FMT> rawn;  // NVFP4: the one after it, requested a tile ahead
   int32_t slot0 = -1;
   {
     const bool mine = ntiles > 0 && kbeg + r < kend;
     const int32_t sspec = mine ? phys_slot(pos0, page0) : -1;
-    if constexpr (FMT == kFmtNvfp4) {
-      if (qu == 0) {
-        // the barrier must see this thread's arrival before the copy's bytes
-        if (sspec >= 0) {
-          mbar_arrive_expect_tx(bar(kBarRows0), kRowBytes);
-          bulk_load(sbase + kOffRaw0 + r * kRawPitch, row_of(sspec), kRowBytes, bar(kBarRows0));
-        } else {
-          mbar_arrive(bar(kBarRows0));
-        }
+    if (qu == 0) {
+      // the barrier must see this thread's arrival before the copy's bytes
+      if (sspec >= 0) {
+        mbar_arrive_expect_tx(bar(kBarRows0), kRB);
+        bulk_load(sbase + kOffRaw0 + r * kRawPitch, row_of(sspec), kRB, bar(kBarRows0));
+      } else {
+        mbar_arrive(bar(kBarRows0));
       }
-    } else {
-      if (sspec >= 0) load_quarter<FMT>(raw, row_of(sspec), qu);
     }
     if (tid == 0) NVMLA_TRACE_POINT(28);
     if (mine) slot0 = classify(pos0, page0, limit, report && qu == 0);
@@ -780,11 +777,27 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
       *reinterpret_cast<uint4*>(smem + kOffQ + c * 8192 + swz(h, q)) = make_uint4(o[0], o[1], o[2], o[3]);
     }
     if (tid == 0) NVMLA_TRACE_POINT(3);
-    if constexpr (FMT == kFmtNvfp4) {
+    {
       // this thread's quarter of its first-tile row, out of shared memory
       ok = ok && wait_bar_warp(bar(kBarRows0), 0, abort_flag, p.err_word);
-      if (ok) {
-        const uint8_t* row = smem + kOffRaw0 + r * kRawPitch;
+      const uint8_t* row = smem + kOffRaw0 + r * kRawPitch;
+      if constexpr (FMT == kFmtFp8) {
+        if (ok) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint4 v = *reinterpret_cast<const uint4*>(row + 128 * qu + 16 * k);
+            raw.c[4 * k] = v.x;
+            raw.c[4 * k + 1] = v.y;
+            raw.c[4 * k + 2] = v.z;
+            raw.c[4 * k + 3] = v.w;
+          }
+          const uint4 rr = *reinterpret_cast<const uint4*>(row + kLatent + 16 * qu);
+          raw.rr[0] = rr.x;
+          raw.rr[1] = rr.y;
+          raw.rr[2] = rr.z;
+          raw.rr[3] = rr.w;
+        }
+      } else if (ok) {
         const uint4 c0 = *reinterpret_cast<const uint4*>(row + 64 * qu);
         const uint4 c1 = *reinterpret_cast<const uint4*>(row + 64 * qu + 16);
         const uint4 c2 = *reinterpret_cast<const uint4*>(row + 64 * qu + 32);
@@ -1151,7 +1164,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
   }
   // the first tile's copies have landed before this CTA's shared memory can go
-  if (tid == 0 && FMT == kFmtNvfp4) wait_bar_drain(bar(kBarRows0), 0);
+  if (tid == 0) wait_bar_drain(bar(kBarRows0), 0);
   if (S > 1) {
     // release / acquire at cluster scope: every CTA's staged partial and
     // (m, l) are visible to every CTA of the cluster
