@@ -283,8 +283,8 @@ def source_hash(names):
     return h.hexdigest()[:16]
 
 
-KERNEL_FILES = {"decode_tc_kernel": ["decode_tc.cu", "common.cuh"],
-                "decode_mma_kernel": ["decode_mma.cu", "common.cuh"]}
+KERNEL_FILES = {"decode_tc_kernel": ["decode_tc.cu", "decode_tc_layout.h", "format.h", "common.cuh"],
+                "decode_mma_kernel": ["decode_mma.cu", "format.h", "common.cuh"]}
 
 
 def traffic_record(kernel):

@@ -80,6 +80,9 @@ typedef enum {
 #define NVMLA_ERRW_BAD_SLOT 0x2    /* block-table slot outside the cache         */
 #define NVMLA_ERRW_PACK_SLOT 0x4   /* pack slot >= num_pages * 64                */
 #define NVMLA_ERRW_WAIT_TIMEOUT 0x8 /* a bounded pipeline wait gave up            */
+#define NVMLA_ERRW_BOUNDS 0x10      /* a library built with NVMLA_DEBUG_BOUNDS found
+                                       an index outside its buffer (never set by the
+                                       default build, which does not check)        */
 
 #define NVMLA_ROW_BYTES 352
 #define NVMLA_FP8_ROW_BYTES 576
@@ -423,6 +426,13 @@ int32_t nvmla_version(void);
 /* Number of kernels this library has launched in this process (all devices,
  * all threads). Lets benchmarks state how many GPU launches a call made. */
 uint64_t nvmla_launch_count(void);
+
+/* How this library was compiled: NVMLA_BUILD_DEBUG_BOUNDS is set in a build
+ * with -DNVMLA_DEBUG_BOUNDS, whose tcgen05 decode checks every data-dependent
+ * index against its buffer and reports a failure as NVMLA_ERRW_BOUNDS (for
+ * tests; slower). The default build sets no flag. */
+#define NVMLA_BUILD_DEBUG_BOUNDS 0x1
+int32_t nvmla_build_flags(void);
 
 #ifdef __cplusplus
 }

@@ -105,6 +105,7 @@ def load():
         "nvmla_last_error": (ctypes.c_char_p, []),
         "nvmla_version": (I32, []),
         "nvmla_launch_count": (ctypes.c_uint64, []),
+        "nvmla_build_flags": (I32, []),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -117,6 +118,15 @@ def load():
 def launch_count() -> int:
     """Kernels the library has launched so far in this process."""
     return int(load().nvmla_launch_count())
+
+
+BUILD_DEBUG_BOUNDS = 0x1
+
+
+def build_flags() -> int:
+    """How the loaded library was compiled (BUILD_DEBUG_BOUNDS: the
+    bounds-checked debug build)."""
+    return int(load().nvmla_build_flags())
 
 
 def _check(status: int):

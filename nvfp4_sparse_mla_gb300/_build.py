@@ -37,7 +37,8 @@ def sources():
 
 
 def _inputs():
-    return sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h"))
+    return (sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h"))
+            + glob.glob(os.path.join(INCLUDE, "*.h")))
 
 
 def is_stale() -> bool:
@@ -47,9 +48,10 @@ def is_stale() -> bool:
     return any(os.path.getmtime(p) > t for p in _inputs())
 
 
-def _compile(src: str, verbose_ptxas: bool) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-    cmd = [nvcc()] + ARCH + CFLAGS + (["-Xptxas", "-v"] if verbose_ptxas else []) + ["-c", src, "-o", obj]
+def _compile(src: str, verbose_ptxas: bool, out_dir: str = BUILD, defines: tuple = ()) -> str:
+    obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
+    cmd = ([nvcc()] + ARCH + CFLAGS + [f"-D{d}" for d in defines] + (["-Xptxas", "-v"] if verbose_ptxas else [])
+           + ["-c", src, "-o", obj])
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc failed on {os.path.basename(src)}:\n{r.stdout}\n{r.stderr}")
@@ -58,18 +60,21 @@ def _compile(src: str, verbose_ptxas: bool) -> str:
     return obj
 
 
-def build(verbose_ptxas: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose_ptxas: bool = False, out_dir: str = BUILD, lib: str = LIB, defines: tuple = ()) -> str:
+    """Compile every csrc/*.cu and link `lib` (the in-tree library unless a
+    variant is asked for: `defines` adds preprocessor switches, e.g. the
+    NVMLA_DEBUG_BOUNDS build, with objects in `out_dir`)."""
+    os.makedirs(out_dir, exist_ok=True)
     srcs = sources()
     with cf.ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas), srcs))
-    tmp = LIB + ".tmp"
+        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas, out_dir, tuple(defines)), srcs))
+    tmp = lib + ".tmp"
     cmd = [nvcc()] + ARCH + ["-shared", "-cudart", "shared", "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 def ensure_built() -> str:

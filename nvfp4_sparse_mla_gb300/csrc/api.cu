@@ -227,6 +227,14 @@ int32_t nvmla_version(void) { return 200; }
 
 uint64_t nvmla_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
+int32_t nvmla_build_flags(void) {
+#ifdef NVMLA_DEBUG_BOUNDS
+  return NVMLA_BUILD_DEBUG_BOUNDS;
+#else
+  return 0;
+#endif
+}
+
 namespace {
 nvmla_status pack_impl(const void* latent_bf16, int64_t latent_stride, const void* rope_bf16, int64_t rope_stride,
                        const int32_t* slot_mapping, int64_t n_tokens, uint8_t* cache, int64_t num_blocks,

@@ -8,19 +8,11 @@
 
 #include <atomic>
 
+#include "format.h"
 #include "nvmla.h"
 
 namespace nvmla {
 
-constexpr int kLatent = 512;
-constexpr int kRope = 64;
-constexpr int kDqk = kLatent + kRope;  // 576
-constexpr int kRowBytes = 352;
-constexpr int kCodeBytes = 256;
-constexpr int kScaleOff = 256;
-constexpr int kRopeOff = 288;
-constexpr int kFp8RowBytes = 576;
-constexpr int kPage = 64;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 

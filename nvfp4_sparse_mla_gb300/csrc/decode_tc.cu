@@ -67,6 +67,24 @@
 // NVMLA_ERRW_WAIT_TIMEOUT, the MMA issuer drains its MMAs, and every thread
 // still takes part in the same cluster barriers, so that every CTA exits.
 #include "common.cuh"
+#include "decode_tc_layout.h"
+
+// A build with -DNVMLA_DEBUG_BOUNDS checks every data-dependent index of the
+// kernel (cache rows, block-table and slot-list entries, output positions,
+// tile and split counts) against its buffer and records a failure as
+// NVMLA_ERRW_BOUNDS in err_word; the shared-memory and TMEM offsets come
+// from decode_tc_layout.h, which a host-compiled test checks exhaustively.
+// The default build compiles the checks away.
+#ifdef NVMLA_DEBUG_BOUNDS
+#define NVMLA_CHECK(cond)                                                \
+  do {                                                                   \
+    if (!(cond)) report_error(p.err_word, NVMLA_ERRW_BOUNDS, 1);          \
+  } while (0)
+#else
+#define NVMLA_CHECK(cond) \
+  do {                    \
+  } while (0)
+#endif
 
 #include <atomic>
 #include <mutex>
@@ -129,59 +147,11 @@ __device__ unsigned long long nvmla_tc_trace[kTraceCtas][kTracePoints];
   } while (0)
 #endif
 
-constexpr int kTile = 128;              // rows per tile (MMA M)
-constexpr int kHeads = 64;              // heads per CTA (MMA N)
-constexpr int kMaxTiles = 16;           // 2048 slots
-constexpr int kThreads = 512;           // 16 warps, all workers
-constexpr int kMmaWarp = 15;            // allocates TMEM; its lane 0 also issues the MMAs
-constexpr int kMaxCluster = 16;         // CTAs sharing one token
-constexpr int kChunkBytes = 16384;      // 128 rows x 64 fp16 dims, 128B-swizzled
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;           // S^T: columns [0, 64)
-constexpr uint32_t kColO = 64;          // O^T block j: columns [64 + 64 j, +64)
-constexpr uint32_t kColR = 320;         // RoPE K: 32 columns (64 fp16 dims x 128 rows)
 constexpr int kPrefetchAhead = 3;       // tiles whose rows are prefetched into L2 ahead of use
 constexpr float kTau = 15.0f;           // rescale threshold, log2 units: P < 2^15 fits fp16
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
-constexpr int kQBytes = kHeads * kDqk * 2;        // raw bf16 query block: 72 KB
-
-// shared memory map (bytes); the base is 1 KB aligned
-constexpr int kOffQ = 0;                              // Q^T: 9 chunks x 8 KB, K-major, swizzled
-constexpr int kOffKV = kOffQ + 9 * 8192;              // latent tile: 8 chunks x 16 KB; first the
-                                                      // first tile's raw rows, last the staged partial
-constexpr int kOffP = kOffKV + 8 * kChunkBytes;       // P^T 16 KB, later the combine weights
-constexpr int kOffSlots = kOffP + kChunkBytes;        // kMaxTiles x 128 int32
-constexpr int kOffRed = kOffSlots + kMaxTiles * kTile * 4;  // 4 quadrants x 64 heads fp32
-constexpr int kOffM = kOffRed + 4 * kHeads * 4;       // 64 fp32 running maxima (log2 units)
-constexpr int kOffAlpha = kOffM + kHeads * 4;         // 64 fp32 rescale factors, later 1 / l
-constexpr int kOffMl = kOffAlpha + kHeads * 4;        // 64 x (m, l) of this CTA
-constexpr int kOffBar = kOffMl + kHeads * 8;
-enum Bar {
-  kBarKV = 0,      // the tile's latent chunks and RoPE K are written (16 warps)
-  kBarS = 1,       // QK done: S^T full; also every earlier MMA done (commit)
-  kBarP = 2,       // P^T written, O^T rescaled if needed (16 warps)
-  kBarPV = 3,      // 4: PV block j done, its two latent chunks reusable (commit)
-  kBarDrain = 7,   // every MMA finished (commit)
-  kBarRows0 = 8,   // the first tile's rows have landed (TMA; one arrival per row)
-  kNumBars = 9
-};
-constexpr int kOffMisc = kOffBar + kNumBars * 8;      // tmem base, abort flag
-constexpr int kSmemBytes = kOffMisc + 16;
-static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(kOffKV % 1024 == 0 && kOffP % 1024 == 0, "swizzled operands need 1 KB alignment");
-static_assert(kQBytes == 9 * 8192, "Q^T is nine 8 KB chunks");
-// The first tile's 128 rows land by TMA in the latent tile's space, an odd
-// number of 16-byte units apart (NVFP4 23, FP8 37), so that the rows of
-// eight consecutive lanes fall into distinct banks
-constexpr int kRawPitchNvfp4 = 368;  // 352-byte rows
-constexpr int kRawPitchFp8 = 592;    // 576-byte rows (37 units of 16 bytes)
-constexpr int kOffRaw0 = kOffKV;
-static_assert(kOffRaw0 + kTile * kRawPitchFp8 <= kOffKV + 8 * kChunkBytes, "first-tile rows fit the latent tile");
-static_assert(kOffMl % 16 == 0, "(m, l) block alignment");
-
-// value dims [dim_lo(r), dim_lo(r + 1)) are combined by CTA r of S: whole
-// groups of 8 dims, so that each CTA's share of a head row is 16-byte units
-__host__ __device__ constexpr int dim_lo(int r, int S) { return 8 * ((r * (kLatent / 8)) / S); }
+// (the shared-memory and TMEM layout, and every offset into them, are in
+// decode_tc_layout.h)
 
 struct Params {
   const __nv_bfloat16* q_latent;
@@ -433,11 +403,6 @@ __device__ __forceinline__ void warp_arrive(uint32_t bar, int lane) {
   if (lane == 0) mbar_arrive(bar);
 }
 
-// swizzled byte offset of 16-byte piece c of row r inside a 128B-swizzled
-// region (rows of 128 bytes, 8-row atoms of 1 KB)
-__device__ __forceinline__ uint32_t swz(int r, int c) {
-  return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
-}
 
 // ---- cluster rank, a barrier over every thread of every CTA with release /
 // acquire semantics at cluster scope, and distributed-shared-memory loads
@@ -597,10 +562,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
   auto bar = [&](int i) { return sbase + kOffBar + 8 * i; };
 
-  const int tile_lo = (static_cast<int>(rank) * p.tiles_total) / S;
-  const int tile_hi = ((static_cast<int>(rank) + 1) * p.tiles_total) / S;
-  const int kbeg = tile_lo * kTile;
-  const int kend = min(tile_hi * kTile, p.topk);
+  const int kbeg = tile_lo(static_cast<int>(rank), S, p.tiles_total) * kTile;
+  const int kend = min(tile_lo(static_cast<int>(rank) + 1, S, p.tiles_total) * kTile, p.topk);
   const int nkeys = max(0, kend - kbeg);
   const int ntiles = (nkeys + kTile - 1) / kTile;  // <= kMaxTiles (host check)
 
@@ -618,11 +581,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
   constexpr int kLaterPer = kMaxTiles / 4;  // later tiles per worker thread
   int32_t posl[kLaterPer];
   {
+    NVMLA_CHECK(S >= 1 && S <= kMaxCluster && ntiles >= 0 && ntiles <= kMaxTiles && kbeg >= 0 && kend <= p.topk);
     if (kbeg + r < kend) pos0 = ldg_nc_s32(tk_row + kbeg + r);
 #pragma unroll
     for (int m = 0; m < kLaterPer; ++m) {
       const int i = 1 + qu + 4 * m;
       const int key = kbeg + i * kTile + r;
+      if (i < ntiles && key < kend) NVMLA_CHECK(key >= 0 && key < p.topk && i < kMaxTiles);
       posl[m] = (i < ntiles && key < kend) ? ldg_nc_s32(tk_row + key) : -1;
     }
   }
@@ -638,8 +603,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
     const uint8_t* ql = reinterpret_cast<const uint8_t*>(p.q_latent + qh0 * kLatent);
     const uint8_t* qr = reinterpret_cast<const uint8_t*>(p.q_rope + qh0 * kRope);
 #pragma unroll
-    for (int m = 0; m < 8; ++m) ldg_nc_v4(ql + 16 * (tid + kThreads * m), qv[m]);
-    ldg_nc_v4(qr + 16 * tid, qv[8]);
+    for (int m = 0; m < 8; ++m) ldg_nc_v4(ql + q_src_off(tid, m), qv[m]);
+    ldg_nc_v4(qr + q_src_off(tid, 8), qv[8]);
   }
   static_assert(kQBytes == 9 * kThreads * 16, "nine 16-byte units of the query block per thread");
   if (tid == 0) {
@@ -655,6 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
   const int32_t* bt_row = p.sel.block_table + static_cast<int64_t>(seq) * p.sel.max_pages;
   auto page_of = [&](int32_t pos) -> int32_t {
     const int32_t pi = min(max(pos >> 6, 0), p.sel.max_pages - 1);
+    NVMLA_CHECK(pi >= 0 && pi < p.sel.max_pages && seq >= 0 && seq < p.sel.num_seqs);
     return ldg_nc_s32(bt_row + pi);
   };
   // slot of position pos given its block-table entry (-1 for padding or a
@@ -680,7 +646,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
     const int64_t s = static_cast<int64_t>(page) * kPage + (pos & 63);
     return s < p.sel.num_slots ? static_cast<int32_t>(s) : -1;
   };
-  auto row_of = [&](int32_t slot) { return p.cache + cache_row_offset(slot, p.sel.page_rows, kRB); };
+  auto row_of = [&](int32_t slot) {
+    NVMLA_CHECK(slot >= 0 && slot < p.sel.num_slots);
+    return p.cache + cache_row_offset(slot, p.sel.page_rows, kRB);
+  };
   int32_t page0 = 0;
   int32_t pagel[kLaterPer];
   if (tid == 0) NVMLA_TRACE_AFTER(25, pos0);
@@ -710,20 +679,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
       // the barrier must see this thread's arrival before the copy's bytes
       if (sspec >= 0) {
         mbar_arrive_expect_tx(bar(kBarRows0), kRB);
-        bulk_load(sbase + kOffRaw0 + r * kRawPitch, row_of(sspec), kRB, bar(kBarRows0));
+        bulk_load(sbase + raw_row_off(r, kRawPitch), row_of(sspec), kRB, bar(kBarRows0));
       } else {
         mbar_arrive(bar(kBarRows0));
       }
     }
     if (tid == 0) NVMLA_TRACE_POINT(28);
     if (mine) slot0 = classify(pos0, page0, limit, report && qu == 0);
-    if (qu == 0) slots[r] = slot0;
+    if (qu == 0) slots[slot_index(0, r)] = slot0;
 #pragma unroll
     for (int m = 0; m < kLaterPer; ++m) {
       const int i = 1 + qu + 4 * m;
       if (i < ntiles) {
         const int32_t sl = classify(posl[m], pagel[m], limit, report);
-        slots[i * kTile + r] = sl;
+        slots[slot_index(i, r)] = sl;
         // the rows of the next three tiles into L2 now, the later ones three
         // tiles ahead of their use (all at once, they would flood the memory
         // system at start-up when a CTA has many tiles)
@@ -766,21 +735,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
     // RoPE unit u holds head u / 8, RoPE dims 8 (u % 8)..+7 (query chunk 8)
 #pragma unroll
     for (int m = 0; m < 9; ++m) {
-      const int u = tid + kThreads * m;
-      const int h = m < 8 ? u >> 6 : tid >> 3;
-      const int c = m < 8 ? (u & 63) >> 3 : 8;
-      const int q = m < 8 ? u & 7 : tid & 7;
       uint32_t o[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e)
         o[e] = pack_f16x2(bf16_bits_to_f32(qv[m][e] & 0xffffu), bf16_bits_to_f32(qv[m][e] >> 16));
-      *reinterpret_cast<uint4*>(smem + kOffQ + c * 8192 + swz(h, q)) = make_uint4(o[0], o[1], o[2], o[3]);
+      *reinterpret_cast<uint4*>(smem + q_dst_off(tid, m)) = make_uint4(o[0], o[1], o[2], o[3]);
     }
     if (tid == 0) NVMLA_TRACE_POINT(3);
     {
       // this thread's quarter of its first-tile row, out of shared memory
       ok = ok && wait_bar_warp(bar(kBarRows0), 0, abort_flag, p.err_word);
-      const uint8_t* row = smem + kOffRaw0 + r * kRawPitch;
+      const uint8_t* row = smem + raw_row_off(r, kRawPitch);
       if constexpr (FMT == kFmtFp8) {
         if (ok) {
 #pragma unroll
@@ -824,20 +789,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
     float lp[16];  // this row's share of its heads' sums
 #pragma unroll
     for (int h = 0; h < 16; ++h) lp[h] = 0.f;
-    uint8_t* chunk0 = smem + kOffKV + (2 * qu) * kChunkBytes;
-    const uint32_t rope_col = tmem + lane_base + kColR + 8 * qu;
+    const uint32_t rope_col = tmem + lane_base + r_col(qu);
     const int hb = 16 * qu;  // first head of this thread's softmax share
     // this thread's part of a tile: latent chunks 2qu, 2qu + 1 of row r into
     // the latent tile, its RoPE dims into TMEM
     auto unpack = [&](bool valid) {
-      store_chunk<FMT>(raw, 0, valid, chunk0, r);
-      store_chunk<FMT>(raw, 1, valid, chunk0 + kChunkBytes, r);
+      store_chunk<FMT>(raw, 0, valid, smem + latent_chunk_off(2 * qu), r);
+      store_chunk<FMT>(raw, 1, valid, smem + latent_chunk_off(2 * qu + 1), r);
       tc_fence_after();
       store_rope<FMT>(raw, valid, rope_col);
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
     };
     // ---- the first tile
-    if (ok && ntiles > 0) unpack(slots[r] >= 0);
+    if (ok && ntiles > 0) unpack(slots[slot_index(0, r)] >= 0);
     if (tid == 0) NVMLA_TRACE_POINT(30);
     if (ok && ntiles > 0) {
       fence_async_smem();
@@ -899,7 +863,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
       if (NVMLA_TRACED_TILE(i)) NVMLA_TRACE_POINT(10 + 8 * NVMLA_TRACE_SLOT(i));
     };
     for (int i = 0; i < ntiles && ok; ++i) {
-      const bool valid = slots[i * kTile + r] >= 0;
+      const bool valid = slots[slot_index(i, r)] >= 0;
       // ---- unpack tile i: chunks 2qu, 2qu + 1 once PV block qu of the
       // previous tile is done; the RoPE K once QK of the previous tile is
       // done (waited for below, in its softmax)
@@ -932,7 +896,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
       tc_fence_after();
       if (tid == 0 && NVMLA_TRACED_TILE(i)) NVMLA_TRACE_POINT(5 + 8 * NVMLA_TRACE_SLOT(i));
       float s[16];
-      tmem_ld16f(tmem + lane_base + kColS + hb, s);
+      tmem_ld16f(tmem + lane_base + s_col(hb), s);
 #pragma unroll
       for (int h = 0; h < 16; ++h) s[h] = valid ? s[h] * p.sl2 : -INFINITY;
       if (i == 0) {
@@ -998,7 +962,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
       }
       // P^T row r, heads hb..hb+15 (pieces 2qu, 2qu + 1); PV of the previous
       // tile has finished reading the buffer (it precedes this tile's QK)
-      uint8_t* pt = smem + kOffP;
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         uint4 q4;
@@ -1006,7 +969,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
         q4.y = pack_f16x2(s[8 * cc + 2], s[8 * cc + 3]);
         q4.z = pack_f16x2(s[8 * cc + 4], s[8 * cc + 5]);
         q4.w = pack_f16x2(s[8 * cc + 6], s[8 * cc + 7]);
-        *reinterpret_cast<uint4*>(pt + swz(r, 2 * qu + cc)) = q4;
+        *reinterpret_cast<uint4*>(smem + pt_off(r, 2 * qu + cc)) = q4;
       }
       if (slow && i >= 1) {
         // O^T to the new maximum: it holds the finished PV of every earlier
@@ -1014,7 +977,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
         // waited for); PV of this tile starts only after kBarP
 #pragma unroll 1
         for (int j = 0; j < 4; ++j) {
-          const uint32_t col = tmem + lane_base + kColO + 64 * j + hb;
+          const uint32_t col = tmem + lane_base + o_col(j, hb);
           float o[16];
           tmem_ld16f(col, o);
 #pragma unroll
@@ -1028,7 +991,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
       warp_arrive(bar(kBarP), lane);
       // ---- a later tile's rows into L2, kPrefetchAhead tiles ahead
       if (qu == 0 && i + 1 + kPrefetchAhead < ntiles) {
-        const int32_t ps = slots[(i + 1 + kPrefetchAhead) * kTile + r];
+        const int32_t ps = slots[slot_index(i + 1 + kPrefetchAhead, r)];
         if (ps >= 0) prefetch_l2(row_of(ps), kRB);
       }
       // ---- rows of later tiles, requested after the softmax so that they do
@@ -1039,16 +1002,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
       // wider FP8 rows keep one.
       if constexpr (FMT == kFmtNvfp4) {
         if (i == 0 && 1 < ntiles) {
-          const int32_t ns = slots[kTile + r];
+          const int32_t ns = slots[slot_index(1, r)];
           if (ns >= 0) load_quarter<FMT>(raw, row_of(ns), qu);
         }
         if (i + 2 < ntiles) {
-          const int32_t ns = slots[(i + 2) * kTile + r];
+          const int32_t ns = slots[slot_index(i + 2, r)];
           if (ns >= 0) load_quarter<FMT>(rawn, row_of(ns), qu);
         }
       } else {
         if (i + 1 < ntiles) {
-          const int32_t ns = slots[(i + 1) * kTile + r];
+          const int32_t ns = slots[slot_index(i + 1, r)];
           if (ns >= 0) load_quarter<FMT>(raw, row_of(ns), qu);
         }
       }
@@ -1086,6 +1049,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
       ml_pub[2 * h] = live ? m_run[h] : -INFINITY;
       ml_pub[2 * h + 1] = live ? l : 0.f;
       alpha_s[h] = live ? 1.f / l : 0.f;
+      NVMLA_CHECK(t < p.T && h0 + h < p.H);
       if (S == 1) p.lse[static_cast<int64_t>(t) * p.H + h0 + h] = live ? (m_run[h] + log2f(l)) * kLn2 : -INFINITY;
     }
     workers_sync();
@@ -1110,8 +1074,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
     for (int j2 = 0; j2 < 4; j2 += 2) {
       float o2[2][16];
       if (have) {
-        NVMLA_TMEM_LD16F(tmem + lane_base + kColO + 64 * j2 + hb, o2[0], 0);
-        NVMLA_TMEM_LD16F(tmem + lane_base + kColO + 64 * (j2 + 1) + hb, o2[1], 0);
+        NVMLA_TMEM_LD16F(tmem + lane_base + o_col(j2, hb), o2[0], 0);
+        NVMLA_TMEM_LD16F(tmem + lane_base + o_col(j2 + 1, hb), o2[1], 0);
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
       } else {
 #pragma unroll
@@ -1122,6 +1086,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
         const int j = j2 + jj;
         const float* o = o2[jj];
         const int d = 128 * j + r;  // TMEM lane r of block j: value dim 128 j + r
+        NVMLA_CHECK(t < p.T && h0 + hb + 15 < p.H && d < kLatent);
         if (S == 1) {
 #pragma unroll
           for (int e = 0; e < 16; ++e)
@@ -1130,7 +1095,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
           // normalised partial (fp16, [dim d][64 heads], 16-byte unit v of
           // dim row d at v ^ (d & 7)) in the latent tile, which the PV no
           // longer reads
-          uint8_t* stg = smem + kOffKV + d * 128;
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {
             uint32_t w4[4];
@@ -1139,7 +1103,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
               const int hl = 8 * cc + 2 * e;
               w4[e] = pack_f16x2(o[hl] * inv_l[hl], o[hl + 1] * inv_l[hl + 1]);
             }
-            *reinterpret_cast<uint4*>(stg + (((2 * qu + cc) ^ (d & 7)) << 4)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            *reinterpret_cast<uint4*>(smem + stage_off(d, 2 * qu + cc)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
           }
         }
       }
@@ -1174,7 +1138,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
     const int D = dim_lo(static_cast<int>(rank) + 1, S) - d0;
     // combine weights l_s 2^(m_s - M) / L per head, [S][64] in the P^T
     // buffer: eight consecutive lanes per head, splits s = q, q + 8
-    float* coef = reinterpret_cast<float*>(smem + kOffP);
     if (tid < 8 * kHeads) {
       const int h = tid >> 3, q = tid & 7;
       float m2[2], l2[2];
@@ -1200,7 +1163,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
       const float inv = L > 0.f ? __frcp_rn(L) : 0.f;
 #pragma unroll
       for (int e = 0; e < 2; ++e)
-        if (q + 8 * e < S) coef[(q + 8 * e) * kHeads + h] = w2[e] * inv;
+        if (q + 8 * e < S) *reinterpret_cast<float*>(smem + coef_off(q + 8 * e, h)) = w2[e] * inv;
       if (rank == 0 && q == 0)
         p.lse[static_cast<int64_t>(t) * p.H + h0 + h] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
     }
@@ -1213,11 +1176,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
     // query block's space (free since the last QK): 8-dim unit c of head h
     // at unit c ^ (h >> 3) of its row, so that the eight head groups a warp
     // writes at once fall into different banks.
-    const int pitch = (D + 63) / 64 * 64;  // bf16 elements per head row of the buffer
+    const int pitch = tb_pitch(D);  // bf16 elements per head row of the buffer
     __nv_bfloat16* tb = reinterpret_cast<__nv_bfloat16*>(smem + kOffQ);
     for (int it = tid; it < D * 8; it += kThreads) {
       const int dd = it >> 3, u = it & 7, d = d0 + dd, v = u ^ (d & 7);
-      const uint32_t off = sbase + kOffKV + d * 128 + u * 16;
+      const uint32_t off = sbase + stage_phys_off(d, u);
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       for (int s0 = 0; s0 < S; s0 += 8) {
         uint4 part[8];
@@ -1228,8 +1191,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
         for (int k = 0; k < 8; ++k) {
           if (s0 + k >= S) break;
           const uint32_t w[4] = {part[k].x, part[k].y, part[k].z, part[k].w};
-          const float4 c0 = *reinterpret_cast<const float4*>(coef + (s0 + k) * kHeads + 8 * v);
-          const float4 c1 = *reinterpret_cast<const float4*>(coef + (s0 + k) * kHeads + 8 * v + 4);
+          const float4 c0 = *reinterpret_cast<const float4*>(smem + coef_off(s0 + k, 8 * v));
+          const float4 c1 = *reinterpret_cast<const float4*>(smem + coef_off(s0 + k, 8 * v + 4));
           const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -1240,7 +1203,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
         }
       }
 #pragma unroll
-      for (int e = 0; e < 8; ++e) tb[(8 * v + e) * pitch + 8 * ((dd >> 3) ^ v) + (dd & 7)] = __float2bfloat16_rn(acc[e]);
+      for (int e = 0; e < 8; ++e) tb[tb_index(8 * v + e, dd, pitch)] = __float2bfloat16_rn(acc[e]);
     }
     if (tid == 0) NVMLA_TRACE_POINT(33);
     __syncthreads();
@@ -1250,8 +1213,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const Params p) 
     const int upr = D / 8;  // 16-byte units per head row
     for (int it = tid; it < kHeads * upr; it += kThreads) {
       const int h = it / upr, c = it - h * upr;
+      NVMLA_CHECK(t < p.T && h0 + h < p.H && d0 + 8 * c + 8 <= kLatent);
       *reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(t) * p.H + h0 + h) * kLatent + d0 + 8 * c) =
-          *reinterpret_cast<const uint4*>(tb + h * pitch + 8 * (c ^ (h >> 3)));
+          *reinterpret_cast<const uint4*>(tb + tb_index(h, 8 * c, pitch));
     }
     if (tid == 0) NVMLA_TRACE_POINT(35);
     // no CTA leaves while another may still read its shared memory

@@ -26,7 +26,7 @@ def test_every_barrier_used_is_initialised():
 
 
 def test_barrier_slots_are_distinct_and_dense():
-    src = _source("decode_tc.cu")
+    src = _source("decode_tc.cu") + _source("decode_tc_layout.h")
     body = re.search(r"enum Bar \{(.*?)\};", src, re.S).group(1)
     values = {n: int(v) for n, v in re.findall(r"(kBar\w+|kNumBars)\s*=\s*(\d+)", body)}
     n_bars = values.pop("kNumBars")

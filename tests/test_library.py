@@ -234,3 +234,10 @@ def test_size_queries_from_eight_threads_at_first_use(lib):
                        timeout=300)
     assert r.returncode == 0, r.stdout + r.stderr
     assert "mismatches 0" in r.stdout
+
+
+def test_in_tree_library_is_the_default_build(lib):
+    """The library the package loads has no debug checks compiled in (the
+    bounds-checked build is a separate variant the GPU tests build)."""
+    assert lib.library_path().endswith("libnvmla.so")
+    assert lib.build_flags() == 0
