@@ -13,8 +13,13 @@
 // order, followed by -1 up to topk. -0.0 ranks as +0.0.
 //
 // One cluster of kTopkCtas CTAs per token, CTA r owning a contiguous chunk of
-// the row. An exact radix select of the k-th largest key over the
-// order-preserving 32-bit image of the scores:
+// the row; the k-th largest key is found exactly, over the order-preserving
+// 32-bit image of the scores. Rows whose chunks fit in shared memory (up to
+// 8 x kResKeys positions, the decode's 200K rows among them) take
+// topk_resident_kernel, described at its definition below: one exchange of
+// the candidates above a bound every CTA can certify. Longer rows take
+// topk_select_kernel, a radix select whose chunk walks read global memory
+// where the chunk does not fit:
 //  * first pass, bits 31-21: each CTA histograms its chunk (keeping the keys
 //    in shared memory where they fit) and adds its non-zero bins into rank
 //    0's cluster histogram (remote shared-memory atomics); rank 0 picks the
@@ -137,7 +142,7 @@ __device__ __forceinline__ void push_hist(cg::cluster_group& cluster, TopkShared
 // rank-`need` key from the top, the count above it and the count in it, as
 // seen by the one thread that finds it (need must lie in 1 .. sum of h).
 // Returns true on that thread. Each bin is cleared after it is read.
-__device__ __forceinline__ bool pick_bin(TopkShared& sh, uint32_t* h, int nb, uint32_t need, uint32_t& bin,
+__device__ __forceinline__ bool pick_bin(uint32_t* warp_tot, uint32_t* h, int nb, uint32_t need, uint32_t& bin,
                                          uint32_t& above, uint32_t& count) {
   const int tid = threadIdx.x;
   // bins from the top: thread i holds bins nb-1-2i and nb-2-2i
@@ -145,7 +150,7 @@ __device__ __forceinline__ bool pick_bin(TopkShared& sh, uint32_t* h, int nb, ui
   const uint32_t h0 = b0 >= 0 ? h[b0] : 0u;
   const uint32_t h1 = b1 >= 0 ? h[b1] : 0u;
   uint32_t total;
-  const uint32_t incl = block_incl_scan(h0 + h1, sh.warp_tot, total);
+  const uint32_t incl = block_incl_scan(h0 + h1, warp_tot, total);
   const uint32_t above0 = incl - h0 - h1, above1 = above0 + h0;
   if (b0 >= 0) h[b0] = 0u;
   if (b1 >= 0) h[b1] = 0u;
@@ -169,7 +174,7 @@ __device__ __forceinline__ bool pick_bin(TopkShared& sh, uint32_t* h, int nb, ui
 // for the next pass.
 __device__ __forceinline__ void pick_broadcast(cg::cluster_group& cluster, TopkShared& sh, int nb, uint32_t need) {
   uint32_t bin, above, count;
-  if (pick_bin(sh, sh.cl_hist, nb, need, bin, above, count)) {
+  if (pick_bin(sh.warp_tot, sh.cl_hist, nb, need, bin, above, count)) {
     for (int r = 0; r < kTopkCtas; ++r) {
       uint32_t* f = cluster.map_shared_rank(sh.found, r);
       f[0] = bin;
@@ -473,7 +478,7 @@ __global__ void __cluster_dims__(kTopkCtas, 1, 1) __launch_bounds__(kTopkThreads
         }
         __syncthreads();
         uint32_t bin, ab, cnt;
-        if (pick_bin(sh, sh.hist, nb, need, bin, ab, cnt)) {
+        if (pick_bin(sh.warp_tot, sh.hist, nb, need, bin, ab, cnt)) {
           sh.found[0] = bin;
           sh.found[1] = ab;
           sh.found[2] = cnt;
@@ -655,21 +660,460 @@ __global__ void __cluster_dims__(kTopkCtas, 1, 1) __launch_bounds__(kTopkThreads
     for (int i = k + tid; i < topk; i += kTopkThreads) o[i] = -1;
 }
 
+// ---------------------------------------------------------------------------
+// Rows whose eighths fit in shared memory (the decode's 200K-position rows):
+// one exchange of candidates instead of rounds of histograms.
+//  * each CTA requests its whole chunk at once, keeps the keys in shared
+//    memory and notes each thread's largest key;
+//  * each CTA picks its own cut b_r: the q-th largest of its per-thread
+//    maxima, q = 2 ceil(k / 8), so that at least q of its keys lie at or
+//    above it (a few hundred on scores like the indexer's);
+//  * each CTA lists its keys >= b_r in position order and copies the list
+//    into a segment of its own in every CTA's pool, with b_r, its count and
+//    its largest key; after one cluster barrier each CTA holds, for
+//    V = max_r b_r, every key >= V of the row. If at least k of them are
+//    >= V, the k-th largest key T is >= V and every key that can be chosen
+//    is in the pool: each CTA finds T over the pool alone (radix passes from
+//    the highest bit where V and the row's largest key differ), counts the
+//    chosen keys of the chunks before its own, and writes its chosen
+//    positions from its own list;
+//  * otherwise (a segment overflowed, or fewer than k keys >= V: bunched
+//    winners, heavy ties) the select runs cluster-wide over every key: three
+//    radix passes whose histograms every CTA adds into every CTA, one
+//    exchange of the per-chunk counts, and an ordered walk of the chunk.
+// Block-wide steps use one-barrier scans: the 32 warp totals are summed by
+// each warp with a warp reduction instead of a second scan.
+constexpr int kResKeys = 32 * 1024;  // longest chunk this kernel takes
+constexpr int kSeg = 1024;           // pool keys per source rank
+static_assert(kResKeys / kTopkThreads <= 32, "a thread's positions of an ordered walk fit one mask");
+static_assert(kSeg <= kTopkThreads, "one listed key per thread in the output step");
+static_assert(kTopkWarps == 32, "one warp total per lane");
+
+struct ResShared {
+  alignas(16) uint32_t keys[kResKeys];          // the chunk's keys, by chunk offset
+  alignas(16) uint32_t pool[kTopkCtas * kSeg];  // rank r's keys >= b_r at [r * kSeg, r * kSeg + seg_n[r])
+  uint32_t lpos[kSeg];                          // chunk offsets of this CTA's listed keys, in order
+  uint32_t hist[2048];                          // this CTA's counts (zero between uses)
+  uint32_t cl_hist[3][2048];                    // fallback: the cluster's counts of pass j
+  uint32_t scan[kTopkWarps];
+  uint32_t cut[kTopkCtas];     // written by rank r: b_r
+  uint32_t top[kTopkCtas];     // written by rank r: its largest key
+  uint32_t seg_n[kTopkCtas];   // written by rank r: its keys >= b_r
+  uint32_t cnt[kTopkCtas][2];  // fallback, written by rank r: its keys above / equal to the threshold
+  uint32_t base[2];            // chosen keys above / equal to the threshold in the chunks before this one
+  uint32_t found[4];
+  uint32_t few[32];
+  uint32_t nfew;
+  uint32_t cmax, cmin;         // largest and smallest per-thread maximum
+};
+static_assert(sizeof(ResShared) <= 227 * 1024, "shared memory of one CTA");
+
+// Exclusive prefix sum of v over the block's threads, in thread order, and
+// the block total; one block barrier. `scan` is written before the barrier
+// and read after it: a barrier must separate two uses of the same array.
+__device__ __forceinline__ uint32_t block_excl_scan1(uint32_t v, uint32_t* scan, uint32_t& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) scan[warp] = x;
+  __syncthreads();
+  const uint32_t wt = scan[lane];
+  total = __reduce_add_sync(0xffffffffu, wt);
+  return __reduce_add_sync(0xffffffffu, lane < warp ? wt : 0u) + x - v;
+}
+
+// Every thread of one CTA: in the nb-bin histogram h (nb <= 2048, a power of
+// two), the bin that holds the rank-`need` key from the top, the count above
+// it and its count, on every thread, and the histogram's total; `bin` is
+// valid only when 1 <= need <= total. Each bin is cleared after it is read.
+// Two block barriers.
+__device__ __forceinline__ uint32_t pick_bin1(ResShared& sh, uint32_t* h, int nb, uint32_t need, uint32_t& bin,
+                                              uint32_t& above, uint32_t& count) {
+  const int tid = threadIdx.x;
+  const int b0 = nb - 1 - 2 * tid, b1 = b0 - 1;  // bins from the top
+  const uint32_t h0 = b0 >= 0 ? h[b0] : 0u;
+  const uint32_t h1 = b1 >= 0 ? h[b1] : 0u;
+  uint32_t total;
+  const uint32_t above0 = block_excl_scan1(h0 + h1, sh.scan, total), above1 = above0 + h0;
+  if (b0 >= 0) h[b0] = 0u;
+  if (b1 >= 0) h[b1] = 0u;
+  if (b0 >= 0 && need > above0 && need <= above1) {
+    sh.found[0] = static_cast<uint32_t>(b0);
+    sh.found[1] = above0;
+    sh.found[2] = h0;
+  }
+  if (b1 >= 0 && need > above1 && need <= above1 + h1) {
+    sh.found[0] = static_cast<uint32_t>(b1);
+    sh.found[1] = above1;
+    sh.found[2] = h1;
+  }
+  __syncthreads();
+  bin = sh.found[0];
+  above = sh.found[1];
+  count = sh.found[2];
+  // (found is next written after the barrier of the next scan, which every
+  // thread reaches only after these reads)
+  return total;
+}
+
+// Mask of the bits above the highest bit where a and b differ (all bits when
+// they are equal), and that bit (-1 when equal).
+__device__ __forceinline__ int common_high_bits(uint32_t a, uint32_t b, uint32_t& mask) {
+  const int hb = a == b ? -1 : 31 - __clz(a ^ b);
+  mask = hb >= 31 ? 0u : 0xffffffffu << (hb + 1);
+  return hb;
+}
+
+__global__ void __cluster_dims__(kTopkCtas, 1, 1) __launch_bounds__(kTopkThreads, 1)
+    topk_resident_kernel(const float* __restrict__ scores, int64_t stride, int32_t ncols,
+                         const int32_t* __restrict__ lengths, int32_t topk, int32_t* __restrict__ out) {
+  extern __shared__ __align__(16) uint8_t topk_smem[];
+  ResShared& sh = *reinterpret_cast<ResShared*>(topk_smem);
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int t = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const float* s = scores + static_cast<int64_t>(t) * stride;
+  int32_t* o = out + static_cast<int64_t>(t) * topk;
+  int L = lengths ? __ldg(lengths + t) : ncols;
+  L = min(max(L, 0), ncols);
+  const int k = min(topk, L);
+  if (k == L) {
+    if (rank == 0)
+      for (int i = tid; i < topk; i += kTopkThreads) o[i] = i < L ? i : -1;
+    return;
+  }
+  const int quads = (L + 3) / 4;
+  const int lo = 4 * ((rank * quads) / kTopkCtas), hi = min(L, 4 * (((rank + 1) * quads) / kTopkCtas));
+  const int len = hi - lo;  // <= kResKeys (host check on the row length)
+  const bool vec = (reinterpret_cast<uintptr_t>(s) & 15u) == 0;
+
+  // ---- the whole chunk requested first (16-byte loads where the row is
+  // aligned); shared memory is cleared while it is on its way
+  constexpr int kU = kResKeys / 4 / kTopkThreads;
+  const float4* s4 = reinterpret_cast<const float4*>(s + lo);
+  const int n4 = vec ? len / 4 : 0;
+  float4 v[kU];
+#pragma unroll
+  for (int r = 0; r < kU; ++r) {
+    const int q = r * kTopkThreads + tid;
+    if (q < n4) v[r] = __ldg(s4 + q);
+  }
+  for (int b = tid; b < 2048; b += kTopkThreads) sh.hist[b] = 0u;
+  if (tid == 0) {
+    sh.nfew = 0u;
+    sh.cmax = 0u;
+    sh.cmin = 0xffffffffu;
+    sh.base[0] = sh.base[1] = 0u;
+  }
+  __syncthreads();
+  // released here, acquired before the first remote access; the loads run
+  // in between
+  cluster_arrive();
+
+  // ---- keys into shared memory; this thread's largest
+  uint32_t tmax = 0u;
+  bool any = false;
+#pragma unroll
+  for (int r = 0; r < kU; ++r) {
+    const int q = r * kTopkThreads + tid;
+    if (q < n4) {
+      const uint4 u = make_uint4(score_key(v[r].x), score_key(v[r].y), score_key(v[r].z), score_key(v[r].w));
+      reinterpret_cast<uint4*>(sh.keys)[q] = u;
+      tmax = max(tmax, max(max(u.x, u.y), max(u.z, u.w)));
+      any = true;
+    }
+  }
+  for (int i = 4 * n4 + tid; i < len; i += kTopkThreads) {  // the tail, or every key of an unaligned row
+    const uint32_t u = score_key(__ldg(s + lo + i));
+    sh.keys[i] = u;
+    tmax = max(tmax, u);
+    any = true;
+  }
+  {
+    const uint32_t wmax = __reduce_max_sync(0xffffffffu, tmax);
+    const uint32_t wmin = __reduce_min_sync(0xffffffffu, any ? tmax : 0xffffffffu);
+    if (lane == 0) {
+      atomicMax(&sh.cmax, wmax);
+      atomicMin(&sh.cmin, wmin);
+    }
+  }
+  const uint32_t holders = __syncthreads_count(any ? 1 : 0);  // also: keys, cmax and cmin are complete
+
+  // ---- this CTA's cut: the q-th largest per-thread maximum, to the low
+  // edge of its bin in one 11-bit digit below the bits that the largest and
+  // smallest maxima share (0 with fewer than q maxima)
+  const uint32_t q = 2u * static_cast<uint32_t>((k + kTopkCtas - 1) / kTopkCtas);
+  uint32_t cut = 0u;
+  if (holders >= q) {
+    uint32_t pmask;
+    const int hb = common_high_bits(sh.cmin, sh.cmax, pmask);
+    if (hb < 0) {
+      cut = sh.cmax;
+    } else {
+      const int w = min(11, hb + 1), sb = hb + 1 - w, nb = 1 << w;
+      if (any) atomicAdd(&sh.hist[(tmax >> sb) & (nb - 1)], 1u);
+      __syncthreads();
+      uint32_t bin, ab, cnt;
+      pick_bin1(sh, sh.hist, nb, q, bin, ab, cnt);
+      cut = (sh.cmax & pmask) | (bin << sb);
+    }
+  }
+
+  // ---- this chunk's keys >= cut, listed in position order (thread i walks
+  // chunk offsets [per i, per (i + 1)), per a multiple of 4)
+  const int per = ((len + kTopkThreads - 1) / kTopkThreads + 3) & ~3;
+  const int p0 = min(tid * per, len), p1 = min(p0 + per, len);
+  uint32_t nlist;  // this chunk's keys >= cut
+  uint32_t* seg = sh.pool + rank * kSeg;
+  {
+    uint32_t fm = 0u;  // bit j: chunk offset p0 + j
+    if (p1 - p0 == per) {
+#pragma unroll
+      for (int j4 = 0; j4 < 32; j4 += 4) {
+        if (j4 < per) {
+          const uint4 u = *reinterpret_cast<const uint4*>(sh.keys + p0 + j4);
+          fm |= ((u.x >= cut ? 1u : 0u) | (u.y >= cut ? 2u : 0u) | (u.z >= cut ? 4u : 0u) | (u.w >= cut ? 8u : 0u))
+                << j4;
+        }
+      }
+    } else {
+      for (int j = 0; j < p1 - p0; ++j) fm |= (sh.keys[p0 + j] >= cut ? 1u : 0u) << j;
+    }
+    uint32_t at = block_excl_scan1(__popc(fm), sh.scan, nlist);
+    while (fm) {
+      const int j = __ffs(fm) - 1;
+      fm &= fm - 1u;
+      if (at < static_cast<uint32_t>(kSeg)) {
+        seg[at] = sh.keys[p0 + j];
+        sh.lpos[at] = static_cast<uint32_t>(p0 + j);
+      }
+      ++at;
+    }
+  }
+  __syncthreads();
+  // ---- the list into every other CTA's pool, with the cut, the count and
+  // the largest key into every CTA
+  cluster_wait();
+  {
+    const int nu = (static_cast<int>(min(nlist, static_cast<uint32_t>(kSeg))) + 3) / 4;
+    for (int u = tid; u < nu; u += kTopkThreads) {
+      const uint4 x = reinterpret_cast<const uint4*>(seg)[u];
+#pragma unroll
+      for (int r = 0; r < kTopkCtas; ++r)
+        if (r != rank) reinterpret_cast<uint4*>(cluster.map_shared_rank(seg, r))[u] = x;
+    }
+    if (tid < kTopkCtas) {
+      cluster.map_shared_rank(sh.seg_n, tid)[rank] = nlist;
+      cluster.map_shared_rank(sh.cut, tid)[rank] = cut;
+      cluster.map_shared_rank(sh.top, tid)[rank] = sh.cmax;
+    }
+  }
+  cluster_barrier();  // every pool is complete
+
+  uint32_t V = 0u, vmax = 0u;
+  bool fast = true;
+#pragma unroll
+  for (int r = 0; r < kTopkCtas; ++r) {
+    V = max(V, sh.cut[r]);
+    vmax = max(vmax, sh.top[r]);
+    fast = fast && sh.seg_n[r] <= static_cast<uint32_t>(kSeg);
+  }
+  // (every CTA computes the same V, vmax, fast, and below the same pool
+  // histograms, so every CTA takes the same path)
+
+  uint32_t prefix = 0u, mask = 0u, need = static_cast<uint32_t>(k);
+  if (fast) {
+    // ---- the k-th largest key among the pool's keys >= V (all of the row's
+    // keys >= V), every CTA on its own copy; they lie in [V, vmax] and share
+    // the bits above the highest bit where V and vmax differ
+    int hb = common_high_bits(V, vmax, mask);
+    prefix = vmax & mask;
+    bool first = true;
+    // (the first pass always runs: it also counts the keys >= V; with
+    // V == vmax it is a one-bit pass that changes nothing else)
+#pragma unroll 1
+    while (first || hb >= 0) {
+      const int w = hb >= 0 ? min(11, hb + 1) : 1, sb = hb >= 0 ? hb + 1 - w : 0, nb = 1 << w;
+#pragma unroll
+      for (int m = 0; m < kTopkCtas; ++m) {
+        const uint32_t u = sh.pool[m * kSeg + tid];
+        if (static_cast<uint32_t>(tid) < sh.seg_n[m] && u >= V && (u & mask) == prefix)
+          atomicAdd(&sh.hist[(u >> sb) & (nb - 1)], 1u);
+      }
+      __syncthreads();
+      uint32_t bin, ab, cnt;
+      const uint32_t total = pick_bin1(sh, sh.hist, nb, need, bin, ab, cnt);
+      if (first && total < need) {  // fewer than k keys >= V
+        fast = false;
+        break;
+      }
+      first = false;
+      prefix |= bin << sb;
+      mask |= static_cast<uint32_t>(nb - 1) << sb;
+      need -= ab;
+      hb = sb - 1;
+      if (hb >= 0 && cnt <= 32u) {
+        // at most 32 keys left in the bin: warp a ranks key a against all
+        for (int m = 0; m < kTopkCtas; ++m) {
+          const uint32_t u = sh.pool[m * kSeg + tid];
+          if (static_cast<uint32_t>(tid) < sh.seg_n[m] && u >= V && (u & mask) == prefix) {
+            const uint32_t c = atomicAdd(&sh.nfew, 1u);
+            if (c < 32u) sh.few[c] = u;
+          }
+        }
+        __syncthreads();
+        const uint32_t nf = min(sh.nfew, 32u);
+        if (static_cast<uint32_t>(warp) < nf) {
+          const uint32_t ua = sh.few[warp];
+          const uint32_t ub = static_cast<uint32_t>(lane) < nf ? sh.few[lane] : 0u;
+          const bool inb = static_cast<uint32_t>(lane) < nf;
+          const uint32_t n_gt = __popc(__ballot_sync(0xffffffffu, inb && ub > ua));
+          const uint32_t n_ge = __popc(__ballot_sync(0xffffffffu, inb && ub >= ua));
+          // (warps holding equal keys write the same values)
+          if (lane == 0 && n_gt < need && need <= n_ge) {
+            sh.found[0] = ua;
+            sh.found[3] = n_gt;
+          }
+        }
+        __syncthreads();
+        prefix = sh.found[0];
+        mask = 0xffffffffu;
+        need -= sh.found[3];
+        break;
+      }
+    }
+  }
+  if (fast) {
+    // ---- chosen keys of the chunks before this one (all >= T >= V: in the pool)
+    uint32_t g = 0u, e = 0u;
+#pragma unroll
+    for (int m = 0; m < kTopkCtas; ++m) {
+      const uint32_t u = sh.pool[m * kSeg + tid];
+      const bool in = m < rank && static_cast<uint32_t>(tid) < sh.seg_n[m];
+      g += in && u > prefix ? 1u : 0u;
+      e += in && u == prefix ? 1u : 0u;
+    }
+    const uint32_t wg = __reduce_add_sync(0xffffffffu, g), we = __reduce_add_sync(0xffffffffu, e);
+    if (lane == 0 && (wg | we) != 0u) {
+      atomicAdd(&sh.base[0], wg);
+      atomicAdd(&sh.base[1], we);
+    }
+    // ---- this chunk's chosen positions, from its list (position order)
+    const bool in = static_cast<uint32_t>(tid) < nlist;
+    const uint32_t u = in ? seg[tid] : 0u;
+    const bool gt = in && u > prefix, eq = in && u == prefix;
+    uint32_t total;
+    const uint32_t c = (gt ? 1u : 0u) | (eq ? 0x10000u : 0u);
+    const uint32_t excl = block_excl_scan1(c, sh.scan, total);  // (its barrier also completes base)
+    const uint32_t gj = sh.base[0] + (excl & 0xffffu), ej = sh.base[1] + (excl >> 16);
+    const uint32_t at = gj + min(ej, need);  // < k when the counts are right; checked all the same
+    if ((gt || (eq && ej < need)) && at < static_cast<uint32_t>(k)) o[at] = lo + static_cast<int>(sh.lpos[tid]);
+  } else {
+    // ---- the select cluster-wide over every key of the row: each pass's
+    // histogram added into every CTA's, then every CTA picks the same bin
+    prefix = 0u;
+    mask = 0u;
+    need = static_cast<uint32_t>(k);
+    for (int b = tid; b < 3 * 2048; b += kTopkThreads) (&sh.cl_hist[0][0])[b] = 0u;
+    for (int b = tid; b < 2048; b += kTopkThreads) sh.hist[b] = 0u;
+    cluster_barrier();  // every CTA's counts are cleared before the first remote add
+#pragma unroll 1
+    for (int pass = 0; pass < 3; ++pass) {
+      const int sb = pass == 0 ? 21 : pass == 1 ? 10 : 0, nb = pass == 2 ? 1024 : 2048;
+      for (int i = tid; i < len; i += kTopkThreads) {
+        const uint32_t u = sh.keys[i];
+        if ((u & mask) == prefix) atomicAdd(&sh.hist[(u >> sb) & (nb - 1)], 1u);
+      }
+      __syncthreads();
+      for (int b = tid; b < nb; b += kTopkThreads) {
+        const uint32_t x = sh.hist[b];
+        if (x != 0u) {
+          sh.hist[b] = 0u;
+#pragma unroll
+          for (int r = 0; r < kTopkCtas; ++r) atomicAdd(cluster.map_shared_rank(sh.cl_hist[pass], r) + b, x);
+        }
+      }
+      cluster_barrier();
+      uint32_t bin, ab, cnt;
+      pick_bin1(sh, sh.cl_hist[pass], nb, need, bin, ab, cnt);
+      prefix |= bin << sb;
+      mask |= static_cast<uint32_t>(nb - 1) << sb;
+      need -= ab;
+    }
+    // this chunk's keys above / equal to the threshold, into every CTA
+    uint32_t n_gt = 0u, n_eq = 0u;
+    for (int i = tid; i < len; i += kTopkThreads) {
+      const uint32_t u = sh.keys[i];
+      n_gt += u > prefix ? 1u : 0u;
+      n_eq += u == prefix ? 1u : 0u;
+    }
+    uint32_t tg;
+    block_excl_scan1(n_gt | (n_eq << 16), sh.scan, tg);  // (each count <= kResKeys < 2^16)
+    if (tid < kTopkCtas) {
+      uint32_t* d = cluster.map_shared_rank(&sh.cnt[0][0], tid) + 2 * rank;
+      d[0] = tg & 0xffffu;
+      d[1] = tg >> 16;
+    }
+    cluster_barrier();  // the last access to another CTA's memory on this path
+    uint32_t base_gt = 0u, base_eq = 0u;
+    for (int r = 0; r < rank; ++r) {
+      base_gt += sh.cnt[r][0];
+      base_eq += sh.cnt[r][1];
+    }
+    // ---- ordered output: thread i walks chunk offsets [per i, per (i + 1))
+    uint32_t gw = 0u, ew = 0u;  // bit j: chunk offset p0 + j
+    for (int j = 0; j < p1 - p0; ++j) {
+      const uint32_t u = sh.keys[p0 + j];
+      gw |= (u > prefix ? 1u : 0u) << j;
+      ew |= (u == prefix ? 1u : 0u) << j;
+    }
+    uint32_t total;
+    const uint32_t c = __popc(gw) | (__popc(ew) << 16);
+    const uint32_t excl = block_excl_scan1(c, sh.scan, total);
+    const uint32_t g = base_gt + (excl & 0xffffu), e = base_eq + (excl >> 16);
+    uint32_t sel = gw | ew;
+    while (sel) {
+      const int j = __ffs(sel) - 1;
+      sel &= sel - 1u;
+      const uint32_t below = (1u << j) - 1u;
+      const uint32_t gj = g + __popc(gw & below), ej = e + __popc(ew & below);
+      const uint32_t at = gj + min(ej, need);
+      if ((((gw >> j) & 1u) || ej < need) && at < static_cast<uint32_t>(k)) o[at] = lo + p0 + j;
+    }
+  }
+  if (rank == kTopkCtas - 1)
+    for (int i = k + tid; i < topk; i += kTopkThreads) o[i] = -1;
+}
+
 cudaError_t launch_topk_select(const float* scores, int64_t stride, int32_t ncols, const int32_t* lengths, int32_t T,
                                int32_t topk, int32_t* out, cudaStream_t stream) {
-  constexpr int kDyn = static_cast<int>(sizeof(TopkShared));
-  // the attribute is set once per device; a caller that sees the flag (acquire)
-  // also sees the attribute set by the caller that raised it (release)
-  static std::atomic<bool> attr_set[kMaxHostDevices];
+  // rows whose longest chunk fits in shared memory take the resident kernel
+  const int64_t quads = (static_cast<int64_t>(ncols) + 3) / 4;
+  const bool resident = 4 * ((quads + kTopkCtas - 1) / kTopkCtas) <= kResKeys;
+  const int dyn = resident ? static_cast<int>(sizeof(ResShared)) : static_cast<int>(sizeof(TopkShared));
+  const void* fn = resident ? reinterpret_cast<const void*>(topk_resident_kernel)
+                            : reinterpret_cast<const void*>(topk_select_kernel);
+  // the attribute is set once per device and kernel; a caller that sees the
+  // flag (acquire) also sees the attribute set by the caller that raised it
+  // (release)
+  static std::atomic<bool> attr_set[2][kMaxHostDevices];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxHostDevices || !attr_set[dev].load(std::memory_order_acquire)) {
-    e = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDyn);
+  std::atomic<bool>* flag = (dev >= 0 && dev < kMaxHostDevices) ? &attr_set[resident ? 1 : 0][dev] : nullptr;
+  if (!flag || !flag->load(std::memory_order_acquire)) {
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < kMaxHostDevices) attr_set[dev].store(true, std::memory_order_release);
+    if (flag) flag->store(true, std::memory_order_release);
   }
-  topk_select_kernel<<<dim3(kTopkCtas, T), kTopkThreads, kDyn, stream>>>(scores, stride, ncols, lengths, topk, out);
+  if (resident)
+    topk_resident_kernel<<<dim3(kTopkCtas, T), kTopkThreads, dyn, stream>>>(scores, stride, ncols, lengths, topk, out);
+  else
+    topk_select_kernel<<<dim3(kTopkCtas, T), kTopkThreads, dyn, stream>>>(scores, stride, ncols, lengths, topk, out);
   return cudaGetLastError();
 }
 

@@ -90,6 +90,19 @@ def test_one_thread_with_many_candidates(lib, cuda):
     check(lib, cuda, s, 2048)
 
 
+def test_one_chunk_lifts_the_cut(lib, cuda):
+    # every 25th position of the first eighth of the row far above the rest:
+    # that CTA's cut lies above them, fewer than k keys of the row do, and
+    # the select falls back to the cluster-wide passes; a second row puts
+    # 3,000 of them in one eighth (more than its list holds)
+    rng = np.random.default_rng(32)
+    s = rng.standard_normal((2, 200_000))
+    s[0, 0:25_000:25] = 100.0 + rng.random(1000)
+    s[1, 100_000:175_000:25] = 50.0 + rng.random(3000)
+    check(lib, cuda, s, 2048)
+    check(lib, cuda, s, 700)
+
+
 def test_rows_not_16_byte_aligned(lib, cuda):
     rng = np.random.default_rng(28)
     s = rng.standard_normal((4, 40_001))
