@@ -103,38 +103,36 @@ nvfp4_pack_kernel(const __nv_bfloat16* __restrict__ latent, int64_t lat_stride,
     const float q = __fdiv_rn(amax, 6.0f);
     const uint32_t sbyte = f32x2_to_e4m3x2(q, 0.f) & 0xffu;
     const float S = __half2float(__ushort_as_half(static_cast<uint16_t>(e4m3x2_to_f16x2(static_cast<uint16_t>(sbyte)) & 0xffffu)));
-    // codes two at a time in bf16x2, straight on the input: every threshold
-    // mid * S (mid = 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5: at most 3
-    // significant bits; S: 4) is exact in bf16. The count of thresholds
-    // below |v| is the code magnitude; at a midpoint the strict or non-strict
-    // comparison sends the value to the even code; a NaN compares false.
+    // codes two at a time in bf16x2, straight on the input. The thresholds
+    // mid_k * S (mid = 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5: at most 3
+    // significant bits; S: 4) are exact bf16 products. The code magnitude is
+    // the count of thresholds below |v|, strictly for even k and non-strictly
+    // for odd k, which sends a midpoint to the even code; the thresholds
+    // increase with k, so the count is found by a binary search: |v| against
+    // mid_3, then mid_1 or mid_5, then one of mid_0, 2, 4, 6, each compare
+    // giving a per-half mask. A NaN compares false (code 0).
+    const uint32_t s2 = (__float_as_uint(S) >> 16) * 0x10001u;
     uint32_t th[7];
     {
-      const float mids[7] = {0.25f, 0.75f, 1.25f, 1.75f, 2.5f, 3.5f, 5.0f};
+      constexpr uint32_t kMid2[7] = {0x3e803e80u, 0x3f403f40u, 0x3fa03fa0u, 0x3fe03fe0u,
+                                     0x40204020u, 0x40604060u, 0x40a040a0u};
 #pragma unroll
-      for (int k = 0; k < 7; ++k) {
-        const uint32_t tb = __float_as_uint(mids[k] * S) >> 16;
-        th[k] = tb | (tb << 16);
-      }
+      for (int k = 0; k < 7; ++k) asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(th[k]) : "r"(s2), "r"(kMid2[k]));
     }
     uint32_t codes[2] = {0u, 0u};
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const uint32_t wi = w[i];
       const uint32_t x2 = wi & 0x7fff7fffu;
-      uint32_t m2 = 0u;  // bf16x2 counts
-#pragma unroll
-      for (int k = 0; k < 7; ++k) {
-        uint32_t c;
-        if (k % 2 == 0)
-          asm("set.gt.bf16x2.bf16x2 %0, %1, %2;" : "=r"(c) : "r"(x2), "r"(th[k]));
-        else
-          asm("set.ge.bf16x2.bf16x2 %0, %1, %2;" : "=r"(c) : "r"(x2), "r"(th[k]));
-        asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(m2) : "r"(m2), "r"(c));
-      }
-      // count + 128 puts the count in the low mantissa bits of each half
-      asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(m2) : "r"(m2), "r"(0x43004300u));
-      m2 = (S == 0.f) ? 0u : (m2 & 0x000f000fu);
+      uint32_t b2, b1, b0;
+      asm("set.ge.u32.bf16x2 %0, %1, %2;" : "=r"(b2) : "r"(x2), "r"(th[3]));
+      const uint32_t t1 = (th[5] & b2) | (th[1] & ~b2);
+      asm("set.ge.u32.bf16x2 %0, %1, %2;" : "=r"(b1) : "r"(x2), "r"(t1));
+      const uint32_t ta = (th[6] & b1) | (th[4] & ~b1), tb = (th[2] & b1) | (th[0] & ~b1);
+      const uint32_t t0 = (ta & b2) | (tb & ~b2);
+      asm("set.gt.u32.bf16x2 %0, %1, %2;" : "=r"(b0) : "r"(x2), "r"(t0));
+      uint32_t m2 = (b2 & 0x00040004u) | (b1 & 0x00020002u) | (b0 & 0x00010001u);
+      m2 = (S == 0.f) ? 0u : m2;
       const uint32_t byte = (m2 & 0xfu) | ((m2 >> 12) & 0xf0u) | ((wi >> 12) & 0x8u) | ((wi >> 24) & 0x80u);
       codes[i >> 2] |= byte << (8 * (i & 3));
     }

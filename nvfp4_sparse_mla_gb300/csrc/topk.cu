@@ -663,14 +663,16 @@ __global__ void __cluster_dims__(kTopkCtas, 1, 1) __launch_bounds__(kTopkThreads
 // ---------------------------------------------------------------------------
 // Rows whose eighths fit in shared memory (the decode's 200K-position rows):
 // one exchange of candidates instead of rounds of histograms.
-//  * each CTA requests its whole chunk at once, keeps the keys in shared
-//    memory and notes each thread's largest key;
+//  * each CTA requests its whole chunk at once, keeps the scores in shared
+//    memory and notes each thread's largest score;
 //  * each CTA picks its own cut b_r: the q-th largest of its per-thread
-//    maxima, q = 2 ceil(k / 8), so that at least q of its keys lie at or
+//    maxima, q = 3 ceil(k / 8) / 2, so that at least q of its keys lie at or
 //    above it (a few hundred on scores like the indexer's);
-//  * each CTA lists its keys >= b_r in position order and copies the list
-//    into a segment of its own in every CTA's pool, with b_r, its count and
-//    its largest key; after one cluster barrier each CTA holds, for
+//  * each CTA lists its keys >= b_r in position order (compared as floats
+//    against the score of b_r; NaN scores are listed whatever their key, and
+//    every later step compares keys) and copies the list into a segment of
+//    its own in every CTA's pool, with b_r, its count and its largest key;
+//    after one cluster barrier each CTA holds, for
 //    V = max_r b_r, every key >= V of the row. If at least k of them are
 //    >= V, the k-th largest key T is >= V and every key that can be chosen
 //    is in the pool: each CTA finds T over the pool alone (radix passes from
@@ -690,7 +692,7 @@ static_assert(kSeg <= kTopkThreads, "one listed key per thread in the output ste
 static_assert(kTopkWarps == 32, "one warp total per lane");
 
 struct ResShared {
-  alignas(16) uint32_t keys[kResKeys];          // the chunk's keys, by chunk offset
+  alignas(16) uint32_t vals[kResKeys];          // the chunk's scores (bits), by chunk offset
   alignas(16) uint32_t pool[kTopkCtas * kSeg];  // rank r's keys >= b_r at [r * kSeg, r * kSeg + seg_n[r])
   uint32_t lpos[kSeg];                          // chunk offsets of this CTA's listed keys, in order
   uint32_t hist[2048];                          // this CTA's counts (zero between uses)
@@ -704,7 +706,8 @@ struct ResShared {
   uint32_t found[4];
   uint32_t few[32];
   uint32_t nfew;
-  uint32_t cmax, cmin;         // largest and smallest per-thread maximum
+  uint32_t cmax, cmin;         // largest and smallest per-thread maximum (keys)
+  uint32_t lmax;               // largest listed key
 };
 static_assert(sizeof(ResShared) <= 227 * 1024, "shared memory of one CTA");
 
@@ -768,6 +771,24 @@ __device__ __forceinline__ int common_high_bits(uint32_t a, uint32_t b, uint32_t
   return hb;
 }
 
+// Wait until the first r + 1 of n committed copy groups have landed (r is a
+// compile-time constant in the unrolled loops that call it).
+template <int N>
+__device__ __forceinline__ void cp_async_wait_dyn(int r) {
+  if constexpr (N > 0) {
+    if (r == 0) {
+      cp_async_wait<N - 1>();
+    } else {
+      cp_async_wait_dyn<N - 1>(r - 1);
+    }
+  }
+}
+
+// The float whose key is `key` (for keys of a float: key(-0) gives +0).
+__device__ __forceinline__ float key_score(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
+
 __global__ void __cluster_dims__(kTopkCtas, 1, 1) __launch_bounds__(kTopkThreads, 1)
     topk_resident_kernel(const float* __restrict__ scores, int64_t stride, int32_t ncols,
                          const int32_t* __restrict__ lengths, int32_t topk, int32_t* __restrict__ out) {
@@ -791,22 +812,25 @@ __global__ void __cluster_dims__(kTopkCtas, 1, 1) __launch_bounds__(kTopkThreads
   const int len = hi - lo;  // <= kResKeys (host check on the row length)
   const bool vec = (reinterpret_cast<uintptr_t>(s) & 15u) == 0;
 
-  // ---- the whole chunk requested first (16-byte loads where the row is
-  // aligned); shared memory is cleared while it is on its way
+  // ---- the whole chunk requested first, straight into shared memory by
+  // 16-byte asynchronous copies where the row is aligned (one commit group
+  // per round of the block's threads; no registers and no L1 lines held);
+  // shared memory is cleared while it is on its way
   constexpr int kU = kResKeys / 4 / kTopkThreads;
   const float4* s4 = reinterpret_cast<const float4*>(s + lo);
   const int n4 = vec ? len / 4 : 0;
-  float4 v[kU];
 #pragma unroll
   for (int r = 0; r < kU; ++r) {
     const int q = r * kTopkThreads + tid;
-    if (q < n4) v[r] = __ldg(s4 + q);
+    if (q < n4) cp_async_16(sh.vals + 4 * q, s4 + q);
+    cp_async_commit();
   }
   for (int b = tid; b < 2048; b += kTopkThreads) sh.hist[b] = 0u;
   if (tid == 0) {
     sh.nfew = 0u;
     sh.cmax = 0u;
     sh.cmin = 0xffffffffu;
+    sh.lmax = 0u;
     sh.base[0] = sh.base[1] = 0u;
   }
   __syncthreads();
@@ -814,25 +838,27 @@ __global__ void __cluster_dims__(kTopkCtas, 1, 1) __launch_bounds__(kTopkThreads
   // in between
   cluster_arrive();
 
-  // ---- keys into shared memory; this thread's largest
-  uint32_t tmax = 0u;
+  // ---- this thread's largest score (as a float: NaN scores are passed
+  // over, which only lowers the cut), each round once its copies landed
+  float fmx = -INFINITY;
   bool any = false;
 #pragma unroll
   for (int r = 0; r < kU; ++r) {
+    cp_async_wait_dyn<kU>(r);
     const int q = r * kTopkThreads + tid;
     if (q < n4) {
-      const uint4 u = make_uint4(score_key(v[r].x), score_key(v[r].y), score_key(v[r].z), score_key(v[r].w));
-      reinterpret_cast<uint4*>(sh.keys)[q] = u;
-      tmax = max(tmax, max(max(u.x, u.y), max(u.z, u.w)));
+      const float4 x = reinterpret_cast<const float4*>(sh.vals)[q];  // (this thread's own copy)
+      fmx = fmaxf(fmx, fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w)));
       any = true;
     }
   }
-  for (int i = 4 * n4 + tid; i < len; i += kTopkThreads) {  // the tail, or every key of an unaligned row
-    const uint32_t u = score_key(__ldg(s + lo + i));
-    sh.keys[i] = u;
-    tmax = max(tmax, u);
+  for (int i = 4 * n4 + tid; i < len; i += kTopkThreads) {  // the tail, or every score of an unaligned row
+    const float x = __ldg(s + lo + i);
+    sh.vals[i] = __float_as_uint(x);
+    fmx = fmaxf(fmx, x);
     any = true;
   }
+  const uint32_t tmax = any ? score_key(fmx) : 0u;
   {
     const uint32_t wmax = __reduce_max_sync(0xffffffffu, tmax);
     const uint32_t wmin = __reduce_min_sync(0xffffffffu, any ? tmax : 0xffffffffu);
@@ -846,7 +872,7 @@ __global__ void __cluster_dims__(kTopkCtas, 1, 1) __launch_bounds__(kTopkThreads
   // ---- this CTA's cut: the q-th largest per-thread maximum, to the low
   // edge of its bin in one 11-bit digit below the bits that the largest and
   // smallest maxima share (0 with fewer than q maxima)
-  const uint32_t q = 2u * static_cast<uint32_t>((k + kTopkCtas - 1) / kTopkCtas);
+  const uint32_t q = (3u * static_cast<uint32_t>((k + kTopkCtas - 1) / kTopkCtas) + 1u) / 2u;
   uint32_t cut = 0u;
   if (holders >= q) {
     uint32_t pmask;
@@ -870,29 +896,37 @@ __global__ void __cluster_dims__(kTopkCtas, 1, 1) __launch_bounds__(kTopkThreads
   uint32_t nlist;  // this chunk's keys >= cut
   uint32_t* seg = sh.pool + rank * kSeg;
   {
+    // key >= cut <=> score >= cf for every score but NaN; !(x < cf) also
+    // lists NaN scores, whose keys the later steps compare
+    const float cf = key_score(cut);
     uint32_t fm = 0u;  // bit j: chunk offset p0 + j
     if (p1 - p0 == per) {
 #pragma unroll
       for (int j4 = 0; j4 < 32; j4 += 4) {
         if (j4 < per) {
-          const uint4 u = *reinterpret_cast<const uint4*>(sh.keys + p0 + j4);
-          fm |= ((u.x >= cut ? 1u : 0u) | (u.y >= cut ? 2u : 0u) | (u.z >= cut ? 4u : 0u) | (u.w >= cut ? 8u : 0u))
+          const float4 x = *reinterpret_cast<const float4*>(sh.vals + p0 + j4);
+          fm |= ((!(x.x < cf) ? 1u : 0u) | (!(x.y < cf) ? 2u : 0u) | (!(x.z < cf) ? 4u : 0u) | (!(x.w < cf) ? 8u : 0u))
                 << j4;
         }
       }
     } else {
-      for (int j = 0; j < p1 - p0; ++j) fm |= (sh.keys[p0 + j] >= cut ? 1u : 0u) << j;
+      for (int j = 0; j < p1 - p0; ++j) fm |= (!(__uint_as_float(sh.vals[p0 + j]) < cf) ? 1u : 0u) << j;
     }
     uint32_t at = block_excl_scan1(__popc(fm), sh.scan, nlist);
+    uint32_t mymax = 0u;
     while (fm) {
       const int j = __ffs(fm) - 1;
       fm &= fm - 1u;
+      const uint32_t u = score_key(__uint_as_float(sh.vals[p0 + j]));
+      mymax = max(mymax, u);
       if (at < static_cast<uint32_t>(kSeg)) {
-        seg[at] = sh.keys[p0 + j];
+        seg[at] = u;
         sh.lpos[at] = static_cast<uint32_t>(p0 + j);
       }
       ++at;
     }
+    const uint32_t wmax = __reduce_max_sync(0xffffffffu, mymax);
+    if (lane == 0 && wmax != 0u) atomicMax(&sh.lmax, wmax);
   }
   __syncthreads();
   // ---- the list into every other CTA's pool, with the cut, the count and
@@ -909,18 +943,24 @@ __global__ void __cluster_dims__(kTopkCtas, 1, 1) __launch_bounds__(kTopkThreads
     if (tid < kTopkCtas) {
       cluster.map_shared_rank(sh.seg_n, tid)[rank] = nlist;
       cluster.map_shared_rank(sh.cut, tid)[rank] = cut;
-      cluster.map_shared_rank(sh.top, tid)[rank] = sh.cmax;
+      cluster.map_shared_rank(sh.top, tid)[rank] = sh.lmax;
     }
   }
   cluster_barrier();  // every pool is complete
 
-  uint32_t V = 0u, vmax = 0u;
-  bool fast = true;
+  // V, the row's largest key (the largest listed one) and whether every
+  // list fit, by warp reductions over lanes 0-7
+  const uint32_t hn = lane < kTopkCtas ? sh.seg_n[lane] : 0u;
+  const uint32_t V = __reduce_max_sync(0xffffffffu, lane < kTopkCtas ? sh.cut[lane] : 0u);
+  const uint32_t vmax = __reduce_max_sync(0xffffffffu, lane < kTopkCtas ? sh.top[lane] : 0u);
+  bool fast = __reduce_max_sync(0xffffffffu, hn) <= static_cast<uint32_t>(kSeg);
+  // this thread's slot of every segment, and which of them hold keys >= V
+  uint32_t pk[kTopkCtas];
+  uint32_t vm = 0u;
 #pragma unroll
-  for (int r = 0; r < kTopkCtas; ++r) {
-    V = max(V, sh.cut[r]);
-    vmax = max(vmax, sh.top[r]);
-    fast = fast && sh.seg_n[r] <= static_cast<uint32_t>(kSeg);
+  for (int m = 0; m < kTopkCtas; ++m) {
+    pk[m] = sh.pool[m * kSeg + tid];
+    vm |= (static_cast<uint32_t>(tid) < __shfl_sync(0xffffffffu, hn, m) && pk[m] >= V ? 1u : 0u) << m;
   }
   // (every CTA computes the same V, vmax, fast, and below the same pool
   // histograms, so every CTA takes the same path)
@@ -939,11 +979,8 @@ __global__ void __cluster_dims__(kTopkCtas, 1, 1) __launch_bounds__(kTopkThreads
     while (first || hb >= 0) {
       const int w = hb >= 0 ? min(11, hb + 1) : 1, sb = hb >= 0 ? hb + 1 - w : 0, nb = 1 << w;
 #pragma unroll
-      for (int m = 0; m < kTopkCtas; ++m) {
-        const uint32_t u = sh.pool[m * kSeg + tid];
-        if (static_cast<uint32_t>(tid) < sh.seg_n[m] && u >= V && (u & mask) == prefix)
-          atomicAdd(&sh.hist[(u >> sb) & (nb - 1)], 1u);
-      }
+      for (int m = 0; m < kTopkCtas; ++m)
+        if (((vm >> m) & 1u) && (pk[m] & mask) == prefix) atomicAdd(&sh.hist[(pk[m] >> sb) & (nb - 1)], 1u);
       __syncthreads();
       uint32_t bin, ab, cnt;
       const uint32_t total = pick_bin1(sh, sh.hist, nb, need, bin, ab, cnt);
@@ -958,11 +995,11 @@ __global__ void __cluster_dims__(kTopkCtas, 1, 1) __launch_bounds__(kTopkThreads
       hb = sb - 1;
       if (hb >= 0 && cnt <= 32u) {
         // at most 32 keys left in the bin: warp a ranks key a against all
+#pragma unroll
         for (int m = 0; m < kTopkCtas; ++m) {
-          const uint32_t u = sh.pool[m * kSeg + tid];
-          if (static_cast<uint32_t>(tid) < sh.seg_n[m] && u >= V && (u & mask) == prefix) {
+          if (((vm >> m) & 1u) && (pk[m] & mask) == prefix) {
             const uint32_t c = atomicAdd(&sh.nfew, 1u);
-            if (c < 32u) sh.few[c] = u;
+            if (c < 32u) sh.few[c] = pk[m];
           }
         }
         __syncthreads();
@@ -992,10 +1029,9 @@ __global__ void __cluster_dims__(kTopkCtas, 1, 1) __launch_bounds__(kTopkThreads
     uint32_t g = 0u, e = 0u;
 #pragma unroll
     for (int m = 0; m < kTopkCtas; ++m) {
-      const uint32_t u = sh.pool[m * kSeg + tid];
-      const bool in = m < rank && static_cast<uint32_t>(tid) < sh.seg_n[m];
-      g += in && u > prefix ? 1u : 0u;
-      e += in && u == prefix ? 1u : 0u;
+      const bool in = m < rank && ((vm >> m) & 1u);
+      g += in && pk[m] > prefix ? 1u : 0u;
+      e += in && pk[m] == prefix ? 1u : 0u;
     }
     const uint32_t wg = __reduce_add_sync(0xffffffffu, g), we = __reduce_add_sync(0xffffffffu, e);
     if (lane == 0 && (wg | we) != 0u) {
@@ -1025,7 +1061,7 @@ __global__ void __cluster_dims__(kTopkCtas, 1, 1) __launch_bounds__(kTopkThreads
     for (int pass = 0; pass < 3; ++pass) {
       const int sb = pass == 0 ? 21 : pass == 1 ? 10 : 0, nb = pass == 2 ? 1024 : 2048;
       for (int i = tid; i < len; i += kTopkThreads) {
-        const uint32_t u = sh.keys[i];
+        const uint32_t u = score_key(__uint_as_float(sh.vals[i]));
         if ((u & mask) == prefix) atomicAdd(&sh.hist[(u >> sb) & (nb - 1)], 1u);
       }
       __syncthreads();
@@ -1047,7 +1083,7 @@ __global__ void __cluster_dims__(kTopkCtas, 1, 1) __launch_bounds__(kTopkThreads
     // this chunk's keys above / equal to the threshold, into every CTA
     uint32_t n_gt = 0u, n_eq = 0u;
     for (int i = tid; i < len; i += kTopkThreads) {
-      const uint32_t u = sh.keys[i];
+      const uint32_t u = score_key(__uint_as_float(sh.vals[i]));
       n_gt += u > prefix ? 1u : 0u;
       n_eq += u == prefix ? 1u : 0u;
     }
@@ -1067,7 +1103,7 @@ __global__ void __cluster_dims__(kTopkCtas, 1, 1) __launch_bounds__(kTopkThreads
     // ---- ordered output: thread i walks chunk offsets [per i, per (i + 1))
     uint32_t gw = 0u, ew = 0u;  // bit j: chunk offset p0 + j
     for (int j = 0; j < p1 - p0; ++j) {
-      const uint32_t u = sh.keys[p0 + j];
+      const uint32_t u = score_key(__uint_as_float(sh.vals[p0 + j]));
       gw |= (u > prefix ? 1u : 0u) << j;
       ew |= (u == prefix ? 1u : 0u) << j;
     }
