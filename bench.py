@@ -864,6 +864,9 @@ def main():
     pack_us = statistics.mean([pk[2 * i].elapsed_time(pk[2 * i + 1]) for i in range(K)]) * 1e3
     pack_bytes = 6144 * (1152 + 352 + 4)
     pack_kernel = kernel_only_us(lambda: nvmla.nvfp4_mla_pack(plat, prope, pslots, pcache), flush)
+    # the same measure of a launch that does no work (torch's GPU sleep for
+    # one cycle): the floor under every kernel-only figure of this line
+    floor = kernel_only_us(lambda: torch.cuda._sleep(1), flush)
 
     # ---------------- the other workloads the baseline names, same protocol
     configs = None
@@ -912,6 +915,8 @@ def main():
                      "frac_kernel": (alg["flops"] / (dec_kernel["cold_l2_us"] * 1e-6) / 1e12) / peak
                      if bound == "tensor" else (alg["bytes"] / (dec_kernel["cold_l2_us"] * 1e-6) / 1e9) / peak},
         "decode_kernel_only": dec_kernel,
+        "kernel_only_floor": dict(floor, what="an empty launch (one-cycle GPU sleep) under the same "
+                                              "kernel-only measure: context, not subtracted"),
         "decode_us": {"mean": dec_us, "median": statistics.median(dec_ms) * 1e3, "min": min(dec_ms) * 1e3},
         "pack_step_us": statistics.mean(pack_ms) * 1e3,
         "pack_chunk": {"tokens": 6144, "bytes": pack_bytes, "us_per_call": pack_us,

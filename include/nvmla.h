@@ -371,9 +371,11 @@ size_t sparse_mla_decode_fp8rows_workspace_size(int32_t T, int32_t H, int32_t to
  *
  * Each row runs on one cluster of 8 CTAs. Rows of up to 262,144 candidates
  * are read from global memory once (each CTA keeps its eighth in shared
- * memory). Slower passes, with the same result, serve longer rows and rows
- * where more than 8,192 scores share the k-th largest score's sign,
- * exponent and two leading mantissa bits.
+ * memory) and need one exchange of candidates between the CTAs. Slower
+ * cluster-wide passes, with the same result, serve rows where a CTA has
+ * more than 1,024 scores at or above its cut, or fewer than k scores lie at
+ * or above the largest cut (winners bunched in one eighth, heavy ties);
+ * longer rows are walked in global memory by a radix select.
  */
 nvmla_status nvmla_topk_select(const float* scores, int64_t row_stride, int32_t ncols,
                                const int32_t* lengths, int32_t T, int32_t topk,
