@@ -103,6 +103,21 @@ def test_one_chunk_lifts_the_cut(lib, cuda):
     check(lib, cuda, s, 700)
 
 
+def test_infinite_scores(lib, cuda):
+    # +inf scores at scattered positions (fewer than k in one row, more
+    # than k in another: ties at +inf taken by lowest position), a row that
+    # is -inf but for 1,000 finite scores (so -inf ties fill the list), and
+    # a row of +inf and -inf only
+    rng = np.random.default_rng(33)
+    s = rng.standard_normal((4, 200_000))
+    s[0, rng.choice(200_000, 300, replace=False)] = np.inf
+    s[1, rng.choice(200_000, 5_000, replace=False)] = np.inf
+    s[2, :] = -np.inf
+    s[2, rng.choice(200_000, 1_000, replace=False)] = rng.standard_normal(1_000)
+    s[3, :] = np.where(rng.random(200_000) < 0.01, np.inf, -np.inf)
+    check(lib, cuda, s, 2048)
+
+
 def test_rows_not_16_byte_aligned(lib, cuda):
     rng = np.random.default_rng(28)
     s = rng.standard_normal((4, 40_001))
