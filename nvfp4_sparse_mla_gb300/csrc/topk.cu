@@ -672,9 +672,9 @@ __global__ void __cluster_dims__(kTopkCtas, 1, 1) __launch_bounds__(kTopkThreads
 //    against the score of b_r; NaN scores are listed whatever their key, and
 //    every later step compares keys) and copies the list into a segment of
 //    its own in every CTA's pool, with b_r, its count and its largest key;
-//    after one cluster barrier each CTA holds, for
-//    V = max_r b_r, every key >= V of the row. If at least k of them are
-//    >= V, the k-th largest key T is >= V and every key that can be chosen
+//    after one cluster barrier each CTA holds, for V = max_r b_r, every key
+//    >= V of the row. If at least k of them are >= V, the k-th largest key
+//    T is >= V and every key that can be chosen
 //    is in the pool: each CTA finds T over the pool alone (radix passes from
 //    the highest bit where V and the row's largest key differ), counts the
 //    chosen keys of the chunks before its own, and writes its chosen
