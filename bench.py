@@ -926,7 +926,11 @@ def main():
                        "frac_hbm_kernel": pack_bytes / (pack_kernel["cold_l2_us"] * 1e-6) / 1e9 / bw},
         "staged": staged,
         "layered": layered,
-        "topk_select": (dict(topk_sel, frac_hbm=topk_sel["gbs"] / bw) if topk_sel else None),
+        "topk_select": (dict(topk_sel, frac_hbm=topk_sel["gbs"] / bw,
+                             frac_hbm_kernel=topk_sel["score_bytes"] / (topk_sel["kernel_only"]["cold_l2_us"] * 1e-6)
+                             / 1e9 / bw,
+                             kernel="topk_resident_kernel (rows of up to 262,144 scores)")
+                        if topk_sel else None),
         "fp8_cache": fp8,
         "configs": configs,
         "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
