@@ -37,6 +37,18 @@ def test_rows_longer_than_shared_memory_holds(lib, cuda):
     check(lib, cuda, s, 2048, lengths=[262_144, 262_148])
 
 
+def test_longest_rows_kept_in_shared_memory(lib, cuda):
+    # 262,144 scores: every CTA's eighth is exactly the 32,768 keys shared
+    # memory holds (every copy round full, every walk's mask full); one more
+    # column and the whole launch takes the global-memory kernel
+    rng = np.random.default_rng(34)
+    s = rng.standard_normal((2, 262_144))
+    check(lib, cuda, s, 2048)
+    check(lib, cuda, s, 2048, lengths=[262_144, 131_071])
+    s1 = rng.standard_normal((2, 262_145))
+    check(lib, cuda, s1, 2048)
+
+
 def test_heavy_ties(lib, cuda):
     rng = np.random.default_rng(22)
     check(lib, cuda, rng.integers(0, 5, (6, 50_000)).astype(np.float64), 2048)
