@@ -11,8 +11,9 @@
 // latent group l (16 values = 32 bytes of bf16, read as two 16-byte loads,
 // so a warp reads the token's 1 KiB latent fully coalesced) and RoPE values
 // 2l, 2l+1. The group's scale and codes are computed in registers without
-// any shuffle; the 352-byte row is assembled in shared memory and written as
-// 22 aligned 16-byte stores.
+// any shuffle, and each lane stores its own bytes of the 352-byte row: 8
+// code bytes, 1 scale byte and 2 RoPE bytes (the warp's three stores cover
+// 256, 32 and 64 contiguous bytes).
 //
 // Rounding, bit-exact with the definition:
 //  * scale = E4M3(amax / 6): fp32 division correctly rounded (__fdiv_rn), then
@@ -54,10 +55,8 @@ nvfp4_pack_kernel(const __nv_bfloat16* __restrict__ latent, int64_t lat_stride,
                   const __nv_bfloat16* __restrict__ rope, int64_t rope_stride,
                   const int32_t* __restrict__ slot_mapping, int64_t n_tokens,
                   uint8_t* __restrict__ cache, int64_t num_slots, int32_t page_rows, int32_t* err_word) {
-  __shared__ __align__(16) uint8_t rowbuf[kPackWarps][kRowBytes];
   const int lane = threadIdx.x & 31;
   const int wib = threadIdx.x >> 5;
-  uint8_t* row = rowbuf[wib];
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kPackWarps;
 
   // a token's values are requested together with its slot (one memory
@@ -136,16 +135,15 @@ nvfp4_pack_kernel(const __nv_bfloat16* __restrict__ latent, int64_t lat_stride,
       const uint32_t byte = (m2 & 0xfu) | ((m2 >> 12) & 0xf0u) | ((wi >> 12) & 0x8u) | ((wi >> 24) & 0x80u);
       codes[i >> 2] |= byte << (8 * (i & 3));
     }
-    *reinterpret_cast<uint2*>(row + 8 * lane) = make_uint2(codes[0], codes[1]);
-    row[kScaleOff + lane] = static_cast<uint8_t>(sbyte);
     // ---- RoPE values 2*lane, 2*lane+1
     const uint16_t r8 = f32x2_to_e4m3x2(bf16_bits_to_f32(rw & 0xffffu), bf16_bits_to_f32(rw >> 16));
-    *reinterpret_cast<uint16_t*>(row + kRopeOff + 2 * lane) = r8;
-    __syncwarp();
-    if (lane < kRowBytes / 16) {
-      reinterpret_cast<uint4*>(cache + cache_row_offset(slot, page_rows))[lane] = reinterpret_cast<const uint4*>(row)[lane];
-    }
-    __syncwarp();
+    // this lane's bytes straight to the row: its 8 code bytes, scale byte
+    // and 2 RoPE bytes (the warp's stores cover 256, 32 and 64 contiguous
+    // bytes)
+    uint8_t* dst = cache + cache_row_offset(slot, page_rows);
+    *reinterpret_cast<uint2*>(dst + 8 * lane) = make_uint2(codes[0], codes[1]);
+    dst[kScaleOff + lane] = static_cast<uint8_t>(sbyte);
+    *reinterpret_cast<uint16_t*>(dst + kRopeOff + 2 * lane) = r8;
   }
 }
 
